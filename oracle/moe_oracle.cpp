@@ -199,8 +199,10 @@ void oracle_load_stats(const oracle_cfg* c, const double* u, const double* s, co
 // [P3] DeepSeek-v2 device-level token drop: C = the average number of assignments a device
 // receives; a device receiving T_d > C keeps its C highest-scored and drops the rest.
 // Readings: D = G virtual devices, device(e) = e / (N/G); one unit is one (token, slot)
-// assignment; C = ceil(T K / D); the score ranked is the routing weight w; ties keep the
-// lower token index, then the lower slot. kept[a] = 1 / 0.
+// assignment; C = ceil(T K / D); the score ranked is the routing weight w, compared as its
+// correctly rounded fp32 value (the precision the kernels keep weights in, so both sides
+// take this integer decision in the same precision); ties keep the lower token index, then
+// the lower slot. kept[a] = 1 / 0.
 void oracle_capacity_drop(const oracle_cfg* c, const int32_t* idx, const double* w,
                           uint8_t* kept) {
   const int T = c->T, K = c->K, D = c->G, per = c->N / c->G;
@@ -213,7 +215,8 @@ void oracle_capacity_drop(const oracle_cfg* c, const int32_t* idx, const double*
       if (idx[a] / per == d) mine.push_back(a);
     if ((long long)mine.size() <= C) continue;
     std::sort(mine.begin(), mine.end(), [&](long long a, long long bb) {
-      if (w[a] != w[bb]) return w[a] > w[bb];
+      const float wa = (float)w[a], wb = (float)w[bb];  // round to nearest even
+      if (wa != wb) return wa > wb;
       return a < bb;  // a = t*K + k: lower token first, then lower slot
     });
     for (size_t j = (size_t)C; j < mine.size(); ++j) kept[mine[j]] = 0;
