@@ -194,6 +194,12 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
  * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK), or MOE_ERR_CUDA if the sync failed. */
 moe_status moe_get_error(moe_stream_t stream);
 
+/* Self-test of the kernels' bounded waits: launches one CTA that waits on an mbarrier nothing
+ * will ever arrive on, with a limit of `timeout_us` microseconds (1 .. 10,000,000). The wait
+ * gives up, records MOE_ERR_TIMEOUT in the device error word and the kernel returns; read it
+ * with moe_get_error(). No fault, no trap, the context stays usable. */
+moe_status moe_selftest_wait_timeout(int32_t timeout_us, moe_stream_t stream);
+
 /* Static text for a status code. */
 const char* moe_status_string(moe_status s);
 

@@ -1,0 +1,98 @@
+// Launchers shared between the C-ABI layer (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- routing (route.cu)
+struct RouteArgs {
+  int T, N, K, G, Gk, topn, score_fn, norm_topk, precise_w;
+  float scale;
+  const float* u;       // [T, N] logits
+  const float* bias;    // [N] selection bias or nullptr
+  int32_t* idx;         // [T, K]
+  float* w;             // [T, K]
+  int* err;
+};
+cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st);
+
+struct StatsArgs {
+  int T, N, K, score_fn;
+  const float* u;       // [T, N]
+  const int32_t* idx;   // [T, K]
+  int32_t* counts;      // [N] (scratch or caller's)
+  float* f;             // [N] or nullptr
+  float* P;             // [N] or nullptr
+  float* lb_z;          // [3] or nullptr
+  float* part_s;        // scratch [nblk, N]
+  double* part_lse;     // scratch [nblk, 2]
+  int nblk;
+  int* err;
+};
+int stats_blocks(int T);
+cudaError_t launch_stats(const StatsArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------- permutation (permute.cu)
+struct PermuteArgs {
+  int T, N, K, D, capacity_drop;
+  const int32_t* idx;   // [T, K]
+  const float* w;       // [T, K]
+  const void* x;        // [T, H] or nullptr
+  int H, elem_bytes;
+  int32_t* offsets;     // [N+1]
+  int32_t* row_token;   // [T*K]
+  int32_t* slot_row;    // [T*K]
+  void* x_perm;         // [T*K, H]
+  // scratch
+  uint32_t* masks;      // [nb, N, 8]
+  int32_t* cnt;         // [nb, N]
+  int32_t* base;        // [nb, N]
+  unsigned long long* thr;  // [D]
+  int* err;
+};
+int permute_blocks(int T);
+cudaError_t launch_permute(const PermuteArgs& a, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- combine (combine.cu)
+struct CombineArgs {
+  int T, H, K, dtype;
+  const void* y;        // [rows, H]
+  const int32_t* slot_row;
+  const float* w;
+  const void* ys;       // [T, H] or nullptr
+  void* out;            // [T, H]
+};
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- GEMMs
+enum GemmMode { MODE_GATE = 0, MODE_UP = 1, MODE_DOWN = 2 };
+
+// Problem set of one grouped GEMM launch: n_routed expert segments (rows from `offsets`,
+// device) plus, when has_shared, one shared-expert problem over all T rows.
+struct GemmArgs {
+  int mode;
+  int T, H, I, S, N;    // N = routed experts (MODE_GATE: router outputs)
+  int n_routed, has_shared;
+  const int32_t* offsets;   // [n_routed+1] device, or nullptr for MODE_GATE
+  int rows_cap;             // rows of the routed A / out tensors (T*K)
+  const void* a0;           // routed A: x_perm [rows_cap,H] | h [rows_cap,I] | x [T,H] (gate)
+  const void* a1;           // shared A: x [T,H] | h_shared [T,S*I]
+  const void* b0;           // routed W: w13 [N,2I,H] | w2 [N,H,I] | w_gate [N,H]
+  const void* b1;           // shared W: w13s [S,2I,H] | w2s [S,H,I]
+  void* out0;               // routed out: h [rows_cap,I] | y [rows_cap,H] | u [T,N] fp32
+  void* out1;               // shared out: h_shared [T,S*I] | y_shared [T,H]
+  const float* gate_bias;   // MODE_GATE: [N] or nullptr
+  int* err;
+};
+// bf16 on tcgen05 / TMEM / TMA (gemm_tc.cu)
+cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st);
+// fp32 on CUDA cores (gemm_simt.cu)
+cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t st);
+
+// Self-test of the bounded wait: one CTA waits on an mbarrier nothing arrives on.
+cudaError_t launch_wait_selftest(int* err, unsigned long long timeout_ns, cudaStream_t st);
+
+}  // namespace moe

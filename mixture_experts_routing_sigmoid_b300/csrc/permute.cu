@@ -1,0 +1,203 @@
+// Token permutation by expert, with the DeepSeek-v2 device-level drop.
+//
+// Kept (token, slot) assignments are laid out as one contiguous segment per expert, experts in
+// ascending order, rows inside a segment in ascending token order (the dispatch that expert
+// parallelism implies: "DeepSeek MoE：从v1到v3的演进", GShard expert parallelism;
+// "DeepSeek-V3的Group-Limited Expert Routing与负载均衡优化实践", section 5, all-to-all).
+// Deterministic, no atomics-order dependence:
+//   1. per 256-token block, a bitmask per expert of the block's tokens that chose it;
+//   2. one CTA scans counts over blocks and experts -> segment offsets, per-block bases;
+//   3. a token's row = base + number of earlier tokens of its block in the expert's mask;
+//   4. one warp per token copies x[t] once to each of its rows.
+// Drop ("DeepSeek MoE：从v1到v3的演进", DeepSeek-v2 device-level token drop): device d of the G
+// virtual devices keeps its C = ceil(T K / G) best assignments by (fp32 weight desc, token asc,
+// slot asc). One CTA per device radix-selects the C-th largest 64-bit key
+// (weight bits << 32 | ~(t K + k)); an assignment is kept iff its key is >= that threshold.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int PB = 256;  // tokens per permutation block
+
+__device__ __forceinline__ unsigned long long drop_key(float w, long long a) {
+  const uint32_t wb = (w > 0.0f) ? __float_as_uint(w) : 0u;  // weights are >= 0
+  return (static_cast<unsigned long long>(wb) << 32) |
+         static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(a));
+}
+
+__global__ void __launch_bounds__(1024) drop_threshold_kernel(PermuteArgs p) {
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned long long s_prefix;
+  __shared__ long long s_remaining;
+  __shared__ unsigned int s_count;
+  const int d = blockIdx.x;
+  const int per = p.N / p.D;
+  const long long A = (long long)p.T * p.K;
+  const long long C = (A + p.D - 1) / p.D;
+  if (threadIdx.x == 0) s_count = 0;
+  __syncthreads();
+  unsigned int mine = 0;
+  for (long long a = threadIdx.x; a < A; a += blockDim.x)
+    if (p.idx[a] / per == d) ++mine;
+  atomicAdd(&s_count, mine);
+  __syncthreads();
+  if ((long long)s_count <= C) {
+    if (threadIdx.x == 0) p.thr[d] = 0ull;  // every key is >= 0: keep all
+    return;
+  }
+  if (threadIdx.x == 0) { s_prefix = 0ull; s_remaining = C; }
+  __syncthreads();
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    const unsigned long long hi_mask = (pass == 0) ? 0ull : (~0ull << (shift + 8));
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const unsigned long long prefix = s_prefix;
+    for (long long a = threadIdx.x; a < A; a += blockDim.x) {
+      if (p.idx[a] / per != d) continue;
+      const unsigned long long key = drop_key(p.w[a], a);
+      if ((key & hi_mask) != prefix) continue;
+      atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long rem = s_remaining, cum = 0;
+      int bin = 0;
+      for (int b = 255; b >= 0; --b) {
+        if (cum + (long long)hist[b] >= rem) { bin = b; break; }
+        cum += hist[b];
+      }
+      s_prefix = prefix | (static_cast<unsigned long long>(bin) << shift);
+      s_remaining = rem - cum;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.thr[d] = s_prefix;
+}
+
+__device__ __forceinline__ bool is_kept(const PermuteArgs& p, long long a, int e) {
+  if (!p.capacity_drop) return true;
+  const int per = p.N / p.D;
+  return drop_key(p.w[a], a) >= p.thr[e / per];
+}
+
+__global__ void __launch_bounds__(PB) perm_hist_kernel(PermuteArgs p) {
+  extern __shared__ uint32_t sm[];  // [N][8]
+  for (int i = threadIdx.x; i < p.N * 8; i += PB) sm[i] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * PB + threadIdx.x;
+  if (t < p.T) {
+    for (int k = 0; k < p.K; ++k) {
+      const long long a = (long long)t * p.K + k;
+      const int e = p.idx[a];
+      if (e < 0 || e >= p.N) { set_error(p.err, ERR_DEVICE_CHECK); continue; }
+      if (is_kept(p, a, e)) atomicOr(&sm[e * 8 + (threadIdx.x >> 5)], 1u << (threadIdx.x & 31));
+    }
+  }
+  __syncthreads();
+  uint32_t* gm = p.masks + (size_t)blockIdx.x * p.N * 8;
+  for (int i = threadIdx.x; i < p.N * 8; i += PB) gm[i] = sm[i];
+  for (int e = threadIdx.x; e < p.N; e += PB) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c += __popc(sm[e * 8 + w]);
+    p.cnt[(size_t)blockIdx.x * p.N + e] = c;
+  }
+}
+
+__global__ void __launch_bounds__(256) perm_scan_kernel(PermuteArgs p, int nb) {
+  __shared__ int tot[256];
+  __shared__ int excl[257];
+  const int e = threadIdx.x;
+  int running = 0;
+  if (e < p.N) {
+    for (int b = 0; b < nb; ++b) {
+      const int c = p.cnt[(size_t)b * p.N + e];
+      p.base[(size_t)b * p.N + e] = running;
+      running += c;
+    }
+  }
+  tot[e] = (e < p.N) ? running : 0;
+  __syncthreads();
+  if (e == 0) {
+    int acc = 0;
+    for (int i = 0; i < p.N; ++i) { excl[i] = acc; acc += tot[i]; }
+    excl[p.N] = acc;
+  }
+  __syncthreads();
+  if (e < p.N) {
+    const int off = excl[e];
+    p.offsets[e] = off;
+    for (int b = 0; b < nb; ++b) p.base[(size_t)b * p.N + e] += off;
+  }
+  if (e == 0) p.offsets[p.N] = excl[p.N];
+}
+
+__global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
+  const int t = blockIdx.x * PB + threadIdx.x;
+  if (t >= p.T) return;
+  const int wi = threadIdx.x >> 5;
+  const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+  for (int k = 0; k < p.K; ++k) {
+    const long long a = (long long)t * p.K + k;
+    const int e = p.idx[a];
+    if (e < 0 || e >= p.N || !is_kept(p, a, e)) { p.slot_row[a] = -1; continue; }
+    const uint32_t* m = p.masks + ((size_t)blockIdx.x * p.N + e) * 8;
+    int rank = __popc(m[wi] & below);
+    for (int i = 0; i < wi; ++i) rank += __popc(m[i]);
+    const int row = p.base[(size_t)blockIdx.x * p.N + e] + rank;
+    p.slot_row[a] = row;
+    p.row_token[row] = t;
+  }
+}
+
+// One warp per token: read x[t] once in 16-byte chunks, write it to every kept row.
+__global__ void __launch_bounds__(256) dispatch_rows_kernel(PermuteArgs p) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const size_t row_bytes = (size_t)p.H * p.elem_bytes;
+  const int chunks = (int)(row_bytes / 16);
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < p.T; t += warps) {
+    const int my = lane < p.K ? p.slot_row[(size_t)t * p.K + lane] : -1;
+    int rows[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) rows[k] = __shfl_sync(FULL_MASK, my, k);
+    const char* src = static_cast<const char*>(p.x) + (size_t)t * row_bytes;
+    char* dst = static_cast<char*>(p.x_perm);
+    for (int c = lane; c < chunks; c += 32) {
+      const uint4 v = ld_nc_v4(src + (size_t)c * 16);
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (k < p.K && rows[k] >= 0) st_v4(dst + (size_t)rows[k] * row_bytes + (size_t)c * 16, v);
+    }
+  }
+}
+
+}  // namespace
+
+int permute_blocks(int T) { return (T + PB - 1) / PB; }
+
+cudaError_t launch_permute(const PermuteArgs& p, int num_sms, cudaStream_t st) {
+  if (p.T <= 0) {
+    // no tokens: empty segments
+    return cudaMemsetAsync(p.offsets, 0, sizeof(int32_t) * (p.N + 1), st);
+  }
+  const int nb = permute_blocks(p.T);
+  if (p.capacity_drop) {
+    drop_threshold_kernel<<<p.D, 1024, 0, st>>>(p);
+  }
+  perm_hist_kernel<<<nb, PB, p.N * 8 * sizeof(uint32_t), st>>>(p);
+  perm_scan_kernel<<<1, 256, 0, st>>>(p, nb);
+  perm_scatter_kernel<<<nb, PB, 0, st>>>(p);
+  if (p.x != nullptr && p.x_perm != nullptr) {
+    int blocks = (p.T + 7) / 8;
+    if (blocks > num_sms * 8) blocks = num_sms * 8;
+    dispatch_rows_kernel<<<blocks, 256, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -20,7 +20,7 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["LayerConfig", "CONFIGS", "make_weights", "make_x", "make_logits",
+__all__ = ["LayerConfig", "CONFIGS", "make_weights", "make_router", "make_x", "make_logits",
            "expert_weights_f64", "to_f64"]
 
 
@@ -122,6 +122,26 @@ def logit_offset(cfg: LayerConfig, g: torch.Generator, device) -> torch.Tensor |
     raise ValueError(cfg.logit_offset)
 
 
+def _router_draws(cfg: LayerConfig, g: torch.Generator, device) -> dict:
+    out = {"w_gate": _randn((cfg.n_routed, cfg.hidden), cfg.gate_std, g, device,
+                            cfg.torch_dtype)}
+    out["gate_logit_bias"] = logit_offset(cfg, g, device)
+    if cfg.has_select_bias:
+        if cfg.select_bias_std > 0:
+            out["select_bias"] = torch.randn((cfg.n_routed,), generator=g, device=device,
+                                             dtype=torch.float32) * cfg.select_bias_std
+        else:
+            out["select_bias"] = torch.zeros((cfg.n_routed,), device=device, dtype=torch.float32)
+    else:
+        out["select_bias"] = None
+    return out
+
+
+def make_router(cfg: LayerConfig, device="cpu", seed: int = 0) -> dict:
+    """w_gate, gate_logit_bias, select_bias: the first draws of make_weights (same values)."""
+    return _router_draws(cfg, _gen(device, seed + 1), device)
+
+
 def make_weights(cfg: LayerConfig, device="cpu", seed: int = 0) -> dict:
     """All layer parameters, in the config dtype (router bias and selection bias in fp32).
 
@@ -138,17 +158,7 @@ def make_weights(cfg: LayerConfig, device="cpu", seed: int = 0) -> dict:
     dt = cfg.torch_dtype
     H, N, S, I = cfg.hidden, cfg.n_routed, cfg.n_shared, cfg.inter
     g = _gen(device, seed + 1)
-    out = {}
-    out["w_gate"] = _randn((N, H), cfg.gate_std, g, device, dt)
-    out["gate_logit_bias"] = logit_offset(cfg, g, device)
-    if cfg.has_select_bias:
-        if cfg.select_bias_std > 0:
-            out["select_bias"] = torch.randn((N,), generator=g, device=device,
-                                             dtype=torch.float32) * cfg.select_bias_std
-        else:
-            out["select_bias"] = torch.zeros((N,), device=device, dtype=torch.float32)
-    else:
-        out["select_bias"] = None
+    out = _router_draws(cfg, g, device)
     out["w13_shared"] = torch.empty((S, 2 * I, H), device=device, dtype=dt)
     out["w2_shared"] = torch.empty((S, H, I), device=device, dtype=dt)
     for s in range(S):

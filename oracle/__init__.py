@@ -157,14 +157,39 @@ def permute(cfg, idx, kept=None):
 
 
 def swiglu_rows(x_rows, w13, w2) -> np.ndarray:
-    x_rows, w13, w2 = _f64(x_rows), _f64(w13), _f64(w2)
+    """SwiGLU expert on rows. Weights: float arrays, or bf16 torch tensors (widened exactly)."""
+    x_rows = _f64(x_rows)
     n, H = x_rows.shape
+    y = np.empty((n, H), np.float64)
+    if _is_bf16_tensor(w13):
+        I = int(w2.shape[1])
+        assert tuple(w13.shape) == (2 * I, H) and tuple(w2.shape) == (H, I)
+        b13 = _bf16_bits(w13)
+        b2 = _bf16_bits(w2)
+        if n:
+            lib().oracle_swiglu_rows_bf16w(n, H, I, _p(x_rows), _p(b13, ctypes.c_uint16),
+                                           _p(b2, ctypes.c_uint16), _p(y))
+        return y
+    w13, w2 = _f64(w13), _f64(w2)
     I = w2.shape[1]
     assert w13.shape == (2 * I, H) and w2.shape == (H, I)
-    y = np.empty((n, H), np.float64)
     if n:
         lib().oracle_swiglu_rows(n, H, I, _p(x_rows), _p(w13), _p(w2), _p(y))
     return y
+
+
+def _is_bf16_tensor(t) -> bool:
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        return False
+    return isinstance(t, torch.Tensor) and t.dtype == torch.bfloat16
+
+
+def _bf16_bits(t) -> np.ndarray:
+    import torch
+    return np.ascontiguousarray(t.detach().to("cpu").contiguous().view(torch.int16).numpy()
+                                .view(np.uint16))
 
 
 def combine(y_rows, slot_row, w, y_shared=None) -> np.ndarray:
@@ -204,8 +229,7 @@ def layer_forward(cfg, x, w_gate, gate_bias, select_bias, expert_weights, shared
     Returns a dict with u, s, idx, w, margin, kept, offsets/row_token/slot_row (full batch
     only), the token list and out [len(tokens), H].
     """
-    x = np.asarray(x)
-    T = x.shape[0]
+    T = x.shape[0]  # x: an array, or any object giving rows through x[row_indices]
     all_tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     route_tokens = np.arange(T) if (cfg.capacity_drop or tokens is None) else all_tokens
     if u is None:

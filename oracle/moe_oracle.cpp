@@ -256,26 +256,50 @@ void oracle_permute(const oracle_cfg* c, const int32_t* idx, const uint8_t* kept
 // the gate projection in rows 0..I-1 and the up projection in rows I..2I-1,
 //   a = x W13[0:I]^T,  g = x W13[I:2I]^T,  h = a * sigmoid(a) * g,  y = h W2^T.
 // Fine-grained segmentation ([P3] DeepSeek-v1, [P2] section 2.1) only changes I and K.
-void oracle_swiglu_rows(int n, int H, int I, const double* x, const double* w13,
-                        const double* w2, double* y) {
-#pragma omp parallel for schedule(dynamic, 1)
+// Weights are read through widen(): double as is, bf16 bit patterns exactly to double.
+// OpenMP splits the independent output features.
+}  // extern "C"
+static inline double widen(double v) { return v; }
+static inline double widen(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof(f));
+  return (double)f;
+}
+template <typename E>
+static void swiglu_rows_impl(int n, int H, int I, const double* x, const E* w13, const E* w2,
+                             double* y) {
+  std::vector<double> hbuf((size_t)n * I);
   for (int r = 0; r < n; ++r) {
     const double* xr = x + (size_t)r * H;
-    std::vector<double> hbuf(I);
+#pragma omp parallel for schedule(static)
     for (int j = 0; j < I; ++j) {
       double a = 0.0, g = 0.0;
       for (int h = 0; h < H; ++h) {
-        a += xr[h] * w13[(size_t)j * H + h];
-        g += xr[h] * w13[(size_t)(I + j) * H + h];
+        a += xr[h] * widen(w13[(size_t)j * H + h]);
+        g += xr[h] * widen(w13[(size_t)(I + j) * H + h]);
       }
-      hbuf[j] = a / (1.0 + std::exp(-a)) * g;
+      hbuf[(size_t)r * I + j] = a / (1.0 + std::exp(-a)) * g;
     }
+#pragma omp parallel for schedule(static)
     for (int o = 0; o < H; ++o) {
       double acc = 0.0;
-      for (int j = 0; j < I; ++j) acc += hbuf[j] * w2[(size_t)o * I + j];
+      for (int j = 0; j < I; ++j) acc += hbuf[(size_t)r * I + j] * widen(w2[(size_t)o * I + j]);
       y[(size_t)r * H + o] = acc;
     }
   }
+}
+extern "C" {
+
+void oracle_swiglu_rows(int n, int H, int I, const double* x, const double* w13,
+                        const double* w2, double* y) {
+  swiglu_rows_impl(n, H, I, x, w13, w2, y);
+}
+
+// Same, with the weights given as bf16 bit patterns.
+void oracle_swiglu_rows_bf16w(int n, int H, int I, const double* x, const uint16_t* w13,
+                              const uint16_t* w2, double* y) {
+  swiglu_rows_impl(n, H, I, x, w13, w2, y);
 }
 
 // Layer output ([P2] section 2.2 forward: shared experts' sum plus routed experts' output;

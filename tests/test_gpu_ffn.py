@@ -1,0 +1,119 @@
+"""Routed + shared SwiGLU experts and the weighted combine on the GPU against the fp64 oracle.
+
+Inputs (x, weights, the permutation) come from the seeded generators and the oracle, never
+from the CUDA path. Expert rows are compared by relative Frobenius error: 1e-2 for bf16
+(tensor cores, h rounded to bf16 between the GEMMs), 1e-5 for fp32.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_inputs import CONFIGS, make_logits, make_router, make_weights, make_x
+from tests.helpers import MID_A, MID_B, MID_V2, rel_frob, sample_tokens, tol_for, workspace
+
+pytestmark = pytest.mark.gpu
+
+CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2}
+
+
+def _perm_inputs(cfg, seed=3):
+    T = cfg.T
+    u = make_logits(cfg, seed=seed, T=T)
+    sb = make_router(cfg)["select_bias"]
+    s = oracle.scores(u.double().numpy(), cfg.score_fn)
+    idx, w, _ = oracle.route(cfg, s, None if sb is None else sb.double().numpy())
+    kept = oracle.capacity_drop(cfg, idx, w) if cfg.capacity_drop else None
+    offs, row_token, slot_row = oracle.permute(cfg, idx, kept)
+    return idx, w, offs, row_token, slot_row
+
+
+def _expert_of_rows(offs):
+    return np.repeat(np.arange(len(offs) - 1), np.diff(offs))
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid_a", "mid_b", "mid_v2", "v1", "v2",
+                                  "v3_prefill", "v3_decode_32", "v3_decode_512"])
+def test_expert_ffn(name):
+    import mixture_experts_routing_sigmoid_b300 as moe
+    cfg = CFGS[name]
+    T, H, K = cfg.T, cfg.hidden, cfg.top_k
+    # oracle cost of every routed row: 3 H I multiply-adds each
+    big = T * K * 3 * H * cfg.inter > 4e9
+    dev = "cuda"
+    w = make_weights(cfg, device=dev)
+    x = make_x(cfg, device=dev, seed=2)
+    idx, wt, offs, row_token, slot_row = _perm_inputs(cfg)
+    R = int(offs[-1])
+    x_perm = torch.zeros((T * K, H), dtype=x.dtype, device=dev)
+    x_perm[:R] = x[torch.from_numpy(row_token).long().to(dev)]
+    y = torch.full((T * K, H), float("nan"), dtype=x.dtype, device=dev)
+    ys = torch.full((T, H), float("nan"), dtype=x.dtype, device=dev) if cfg.n_shared else None
+    ws = workspace(cfg, T)
+    moe.moe_expert_ffn(cfg, T, x_perm, torch.from_numpy(offs).to(dev), x, w, y, ys, ws)
+    assert moe.moe_get_error() == 0
+
+    # routed rows: all of them on small layers, a sample spread over experts on big ones
+    exp_of = _expert_of_rows(offs)
+    rows = np.arange(R) if not big else np.unique(np.concatenate(
+        [offs[:-1][np.diff(offs) > 0],                       # first row of every segment
+         offs[1:][np.diff(offs) > 0] - 1,                    # last row (ragged tails)
+         np.random.default_rng(0).choice(R, 64, replace=False)]))
+    if big:
+        # keep the oracle cost bounded: at most 48 distinct experts
+        ex = np.unique(exp_of[rows])[:48]
+        rows = rows[np.isin(exp_of[rows], ex)]
+    got = y[torch.from_numpy(rows).long().to(dev)].double().cpu().numpy()
+    want = np.zeros_like(got)
+    xr = x_perm[torch.from_numpy(rows).long().to(dev)].double().cpu().numpy()
+    for e in np.unique(exp_of[rows]):
+        sel = exp_of[rows] == e
+        w13, w2 = (w["w13"][e], w["w2"][e]) if cfg.dtype == "bf16" else \
+            (w["w13"][e].double().cpu().numpy(), w["w2"][e].double().cpu().numpy())
+        want[sel] = oracle.swiglu_rows(xr[sel], w13, w2)
+    err = rel_frob(got, want)
+    assert err <= tol_for(cfg), f"routed rows: rel err {err:.3g}"
+
+    if cfg.n_shared:
+        tok = sample_tokens(T, 32 if big else T, seed=1)
+        xs = x[torch.from_numpy(tok).long().to(dev)].double().cpu().numpy()
+        want_s = np.zeros((len(tok), H))
+        for s_ in range(cfg.n_shared):
+            w13, w2 = (w["w13_shared"][s_], w["w2_shared"][s_]) if cfg.dtype == "bf16" else \
+                (w["w13_shared"][s_].double().cpu().numpy(), w["w2_shared"][s_].double().cpu().numpy())
+            want_s += oracle.swiglu_rows(xs, w13, w2)
+        got_s = ys[torch.from_numpy(tok).long().to(dev)].double().cpu().numpy()
+        err = rel_frob(got_s, want_s)
+        assert err <= tol_for(cfg), f"shared rows: rel err {err:.3g}"
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid_b", "mid_v2", "v3_prefill"])
+def test_combine(name):
+    import mixture_experts_routing_sigmoid_b300 as moe
+    cfg = CFGS[name]
+    T, H, K = cfg.T, cfg.hidden, cfg.top_k
+    idx, wt, offs, row_token, slot_row = _perm_inputs(cfg)
+    R = int(offs[-1])
+    g = torch.Generator(device="cuda").manual_seed(5)
+    y = torch.randn((max(R, 1), H), generator=g, device="cuda").to(cfg.torch_dtype)
+    ys = torch.randn((T, H), generator=g, device="cuda").to(cfg.torch_dtype)
+    w32 = wt.astype(np.float32)
+    out = torch.empty((T, H), dtype=cfg.torch_dtype, device="cuda")
+    moe.moe_combine(cfg, T, y, torch.from_numpy(slot_row).cuda(), torch.from_numpy(w32).cuda(),
+                    ys, out)
+    assert moe.moe_get_error() == 0
+    tok = sample_tokens(T, 256, seed=2)
+    # only the rows the sampled tokens reference, renumbered
+    sr = slot_row[tok]
+    used = np.unique(sr[sr >= 0])
+    remap = -np.ones(max(R, 1), np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    sr_sub = np.where(sr >= 0, remap[np.maximum(sr, 0)], -1).astype(np.int32)
+    y_sub = y[torch.from_numpy(used).long().cuda()].double().cpu().numpy()
+    want = oracle.combine(y_sub, sr_sub, w32[tok].astype(np.float64),
+                          ys[torch.from_numpy(tok).long().cuda()].double().cpu().numpy())
+    got = out[torch.from_numpy(tok).long().cuda()].double().cpu().numpy()
+    assert rel_frob(got, want) <= (1e-2 if cfg.dtype == "bf16" else 1e-6)
+    if cfg.dtype == "bf16":
+        # output is the bf16 rounding of an fp32 sum: elementwise within 2^-8 relative + slack
+        assert np.all(np.abs(got - want) <= 2 ** -8 * np.abs(want) + 1e-2)

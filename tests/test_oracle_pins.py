@@ -362,3 +362,14 @@ def test_bias_update_sign_rule():
     counts = np.array([10, 2, 6, 6])  # mean 6
     b = oracle.bias_update(counts, 0.001, np.zeros(4))
     np.testing.assert_array_equal(b, [-0.001, 0.001, 0.0, 0.0])
+
+
+def test_swiglu_bf16_weights_equal_widened_f64():
+    """The bf16-weight entry widens exactly: same result as the fp64 entry on the same values."""
+    g = torch.Generator().manual_seed(19)
+    x = torch.randn((3, 64), generator=g, dtype=torch.float64).numpy()
+    w13 = (torch.randn((2 * 32, 64), generator=g) * 0.1).to(torch.bfloat16)
+    w2 = (torch.randn((64, 32), generator=g) * 0.1).to(torch.bfloat16)
+    a = oracle.swiglu_rows(x, w13, w2)
+    b = oracle.swiglu_rows(x, w13.to(torch.float64).numpy(), w2.to(torch.float64).numpy())
+    np.testing.assert_array_equal(a, b)
