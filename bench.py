@@ -1,0 +1,409 @@
+"""Benchmark: MoE-layer tokens/s (route + permute + expert FFN + combine) on B300, with the
+roofline fraction of the dominant kernel and the fp64 oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3_prefill] [--impl ours|reference]
+
+One step = one moe_layer_forward (gate GEMM, routing, permutation, routed + shared SwiGLU
+experts, combine) over one batch of synthetic inputs already resident in HBM. N > 1 runs N
+independent replicas (one per GPU, launched by torch.distributed.run), weak scaling: the layer
+forward of one GPU's batch has no cross-GPU exchange.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (route+permute+expert FFN+combine); % of roofline"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--config", default="v3_prefill")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-stages", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """Slowest rank's value (the job takes as long as its slowest replica)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- peaks, clocks
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.lines, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- work accounting
+def layer_work(cfg, counts, kept_rows: int) -> dict:
+    """Algorithmic FLOPs and bytes of one layer forward (no credit for permutation copies)."""
+    T, H, N, I, S, K = cfg.T, cfg.hidden, cfg.n_routed, cfg.inter, cfg.n_shared, cfg.top_k
+    eb = cfg.elem_bytes
+    touched = int(sum(1 for c in counts if c > 0))
+    flops = 2.0 * T * H * N + 6.0 * H * I * (kept_rows + T * S)
+    bytes_ = (2.0 * T * H * eb + N * H * eb + (touched + S) * 3.0 * H * I * eb
+              + T * N * 4.0 + T * K * 8.0)
+    return dict(flops=flops, bytes=bytes_, touched=touched,
+                up_flops=4.0 * H * I * (kept_rows + T * S),
+                down_flops=2.0 * H * I * (kept_rows + T * S),
+                up_weight_bytes=(touched + S) * 2.0 * H * I * eb,
+                down_weight_bytes=(touched + S) * 1.0 * H * I * eb,
+                weight_bytes=(touched + S) * 3.0 * H * I * eb)
+
+
+def workload_name(cfg) -> str:
+    return (f"{cfg.name}: T={cfg.T} H={cfg.hidden} N={cfg.n_routed} G={cfg.n_groups} "
+            f"Gk={cfg.topk_groups} K={cfg.top_k} S={cfg.n_shared} I={cfg.inter} "
+            f"{cfg.score_fn} {cfg.dtype}")
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import mixture_experts_routing_sigmoid_b300 as moe
+    from moe_inputs import CONFIGS, make_weights, make_x
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = CONFIGS[args.config]
+    T, H, K, N = cfg.T, cfg.hidden, cfg.top_k, cfg.n_routed
+    w = make_weights(cfg, device=dev, seed=0)
+    x = make_x(cfg, device=dev, seed=0)
+    out = torch.empty_like(x)
+    ws = torch.empty(moe.moe_workspace_size(cfg, T), dtype=torch.uint8, device=dev)
+    want_stats = cfg.name == "v1"  # the v1 layer also reports f, P, L_B, L_Z
+    counts = torch.empty(N, dtype=torch.int32, device=dev)
+    lbz = torch.empty(3, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # gate, route, permute (hist, scan, scatter, dispatch), up, down, combine (+ drop, + stats)
+    launches_per_step = 9 + (1 if cfg.capacity_drop else 0) + (3 if want_stats else 0)
+
+    def step():
+        moe.moe_layer_forward(cfg, T, x, w, out, counts if want_stats else None,
+                              lbz if want_stats else None, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    st = moe.moe_get_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error {st} during warm-up")
+
+    # ---- device-timed region (inputs resident in HBM; expert weights far above L2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    st = moe.moe_get_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error {st} in the timed region")
+    ms_max = max_over_ranks(ms, world, dev)
+    ms_step = ms_max / args.steps
+    tok_s = world * T * args.steps / (ms_max / 1e3)
+
+    # routing outcome of this batch (for the work accounting)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, K), dtype=torch.float32, device=dev)
+    moe.moe_route(cfg, T, x, w, None, None, idx, wt, ws, stream)
+    offs = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    rt = torch.empty(T * K, dtype=torch.int32, device=dev)
+    sr = torch.empty(T * K, dtype=torch.int32, device=dev)
+    moe.moe_permute(cfg, T, idx, wt, None, offs, rt, sr, None, ws, stream)
+    offs_h = offs.cpu().numpy()
+    kept_rows = int(offs_h[-1])
+    work = layer_work(cfg, np.diff(offs_h), kept_rows)
+    pk = peaks()
+
+    result = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+        "config": {"workload": workload_name(cfg), "T": T, "hidden": H, "n_routed": N,
+                   "top_k": K, "n_shared": cfg.n_shared, "inter": cfg.inter,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (routed expert weights %.1f GB)" %
+                         (w["w13"].numel() * 2 * 1.5 / 1e9),
+                   "kept_rows": kept_rows, "touched_experts": work["touched"]},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    t_flop = work["flops"] / (pk["bf16"] * 1e12)
+    t_byte = work["bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_roof = max(t_flop, t_byte)
+    result["layer_roofline"] = {
+        "flops": work["flops"], "bytes": work["bytes"], "roofline_ms": t_roof * 1e3,
+        "frac": t_roof * 1e3 / ms_step, "tflops": work["flops"] / (ms_step * 1e-3) / 1e12,
+        "weight_gbs": work["weight_bytes"] / (ms_step * 1e-3) / 1e9,
+        "bound": "tensor" if t_flop >= t_byte else "hbm", "peaks": pk["source"] + " burst"}
+    result["clocks"] = clk.summary()
+
+    # ---- per-kernel timing of the two expert GEMMs, live, on the launching stream
+    if not args.no_stages:
+        x_perm = torch.empty((T * K, H), dtype=x.dtype, device=dev)
+        h = torch.empty((T * K, cfg.inter), dtype=x.dtype, device=dev)
+        h_sh = torch.empty((T, max(cfg.n_shared, 1) * cfg.inter), dtype=x.dtype, device=dev)
+        y = torch.empty((T * K, H), dtype=x.dtype, device=dev)
+        y_sh = torch.empty((T, H), dtype=x.dtype, device=dev)
+        moe.moe_permute(cfg, T, idx, wt, x, offs, rt, sr, x_perm, ws, stream)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        up_ms, down_ms = [], []
+        shp = cfg.n_shared > 0
+        for i in range(args.warmup + args.steps):
+            evs[0].record(stream)
+            moe.moe_expert_up(cfg, T, x_perm, offs, x, w, h, h_sh if shp else None, stream)
+            evs[1].record(stream)
+            moe.moe_expert_down(cfg, T, h, offs, h_sh if shp else None, w, y,
+                                y_sh if shp else None, stream)
+            evs[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= args.warmup:
+                up_ms.append(evs[0].elapsed_time(evs[1]))
+                down_ms.append(evs[1].elapsed_time(evs[2]))
+        up = statistics.mean(up_ms)
+        dn = statistics.mean(down_ms)
+        up_tf = work["up_flops"] / (up * 1e-3) / 1e12
+        if result["layer_roofline"]["bound"] == "tensor":
+            result["roofline"] = {
+                "kernel": "tc_gemm_kernel<MODE_UP> (grouped SwiGLU up projection, tcgen05)",
+                "bound": "tensor", "achieved": up_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": up_tf / pk["bf16"], "traffic": None,
+                "peak_kind": "bf16 burst, " + pk["source"],
+                "frac_of_sustained": up_tf / pk["bf16_sus"], "avg_launch_ms": up,
+                "algorithmic_flops_per_launch": work["up_flops"]}
+        else:
+            gbs = work["up_weight_bytes"] / (up * 1e-3) / 1e9
+            result["roofline"] = {
+                "kernel": "tc_gemm_kernel<MODE_UP> (grouped SwiGLU up projection, tcgen05)",
+                "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                "peak_kind": "HBM copy, " + pk["source"], "avg_launch_ms": up,
+                "algorithmic_bytes_per_launch": work["up_weight_bytes"]}
+        result["kernels"] = {
+            "up_ms": up, "down_ms": dn, "up_tflops": up_tf,
+            "down_tflops": work["down_flops"] / (dn * 1e-3) / 1e12,
+            "up_share_of_step": up / ms_step, "down_share_of_step": dn / ms_step}
+        del x_perm, h, h_sh, y, y_sh
+
+    # ---- end to end through the C ABI: pinned host x in, host out back, every step
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        xd = torch.empty_like(x)
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                barrier(world)
+                torch.cuda.synchronize(dev)
+                ev0.record(stream)
+            xd.copy_(xh, non_blocking=True)
+            moe.moe_layer_forward(cfg, T, xd, w, out, None, None, ws, stream)
+            oh.copy_(out, non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+        result["e2e"] = {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                         "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+                         "d2h_bytes_per_step": oh.numel() * oh.element_size()}
+
+    # ---- the oracle on the host cores (rank 0, N = 1 only), bounded sample
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = oracle_baseline(cfg, x, w, n_tokens=32, steps=1)
+    return result
+
+
+def oracle_baseline(cfg, x, w, n_tokens: int, steps: int, seed: int = 0) -> dict:
+    """Time the fp64 oracle (as it stands) on `steps` samples of `n_tokens` tokens each.
+
+    The experts a sample touches are copied to host memory before its timed call."""
+    import numpy as np
+    import torch
+
+    import oracle
+    rng = np.random.default_rng(seed)
+    f64 = (lambda t: None if t is None else t.double().cpu().numpy())
+    wg, gb, sb = f64(w["w_gate"]), f64(w["gate_logit_bias"]), f64(w["select_bias"])
+    host = {}
+    for s_ in range(cfg.n_shared):
+        host[("s", s_)] = (w["w13_shared"][s_].cpu(), w["w2_shared"][s_].cpu())
+    ew = (lambda e: host[("r", e)])
+    sw = (lambda s: host[("s", s)])
+    total_s, total_tok = 0.0, 0
+    xs_all = f64(x) if cfg.capacity_drop else None
+    for _ in range(steps):
+        tok = np.sort(rng.choice(cfg.T, size=min(n_tokens, cfg.T), replace=False))
+        # untimed: route the sample once to learn which experts to stage on the host
+        xr = f64(x[torch.as_tensor(tok).long().to(x.device)])
+        u = oracle.gate_logits(xs_all if cfg.capacity_drop else xr, wg, gb)
+        idx, _, _ = oracle.route(cfg.replace(T=u.shape[0]), oracle.scores(u, cfg.score_fn), sb)
+        for e in np.unique(idx):
+            if ("r", int(e)) not in host:
+                host[("r", int(e))] = (w["w13"][int(e)].cpu(), w["w2"][int(e)].cpu())
+        t0 = time.perf_counter()
+        if cfg.capacity_drop:
+            oracle.layer_forward(cfg, xs_all, wg, gb, sb, ew, sw, tokens=tok)
+        else:
+            oracle.layer_forward(cfg.replace(T=len(tok)), xr, wg, gb, sb, ew, sw)
+        total_s += time.perf_counter() - t0
+        total_tok += len(tok)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": total_tok / total_s, "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{steps} x {n_tokens} random tokens of the {cfg.name} batch: gate logits, "
+                      f"routing, {cfg.top_k} routed + {cfg.n_shared} shared SwiGLU experts and "
+                      f"the combine in fp64 (touched expert weights staged in host memory)"
+                      + ("; gate and routing over the whole batch for the drop"
+                         if cfg.capacity_drop else ""),
+            "seconds": total_s}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, world, rank, local):
+    """The oracle, as it stands, on the host cores: same metric / unit / config as our arm."""
+    import torch
+    from moe_inputs import CONFIGS, make_weights, make_x
+    cfg = CONFIGS[args.config]
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    w = make_weights(cfg, device=dev, seed=0)
+    x = make_x(cfg, device=dev, seed=0)
+    n_tok = 4
+    if args.warmup:
+        oracle_baseline(cfg, x, w, n_tokens=n_tok, steps=1, seed=99)
+    cb = oracle_baseline(cfg, x, w, n_tokens=n_tok, steps=args.steps, seed=1)
+    ms_step = cb["seconds"] / args.steps * 1e3
+    return {"metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+            "config": {"workload": workload_name(cfg), "T": cfg.T, "hidden": cfg.hidden,
+                       "n_routed": cfg.n_routed, "top_k": cfg.top_k,
+                       "n_shared": cfg.n_shared, "inter": cfg.inter,
+                       "parallelism": "host cores"},
+            "impl": "reference",
+            "cpu_baseline": {"value": cb["value"], "unit": "tokens/s", "cores": cb["cores"],
+                             "kind": "oracle", "sample": cb["sample"]},
+            "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank, local)), flush=True)
+    else:
+        res = run_ours(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -58,7 +58,7 @@ class MoeWeights(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m mixture_experts_routing_sigmoid_b300.build`")
+                          "`python mixture_experts_routing_sigmoid_b300/build.py`")
     L = ctypes.CDLL(LIB_PATH)
     P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     CFG, W = ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights)

@@ -19,8 +19,8 @@ def _declared_functions():
 
 @pytest.fixture(scope="module")
 def moe():
-    from mixture_experts_routing_sigmoid_b300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import mixture_experts_routing_sigmoid_b300 as m
     return m
 
