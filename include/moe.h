@@ -150,6 +150,25 @@ moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_idx
                        moe_stream_t stream);
 
 /*
+ * moe_permute without a workspace, for callers that cannot allocate device memory (a runtime
+ * without a device allocator, a host framework that owns all device allocations and gives none
+ * to plugins, a process that must not grow its device footprint). The pages have no
+ * counterpart: this is a deployment variant of moe_permute, same arguments minus ws, same
+ * outputs bit for bit.
+ *   Its scratch (per-block expert bitmasks, counts, segment bases, drop thresholds) is one
+ *   file-scope device array of 2.5 MiB that every GPU loading the library holds until exit.
+ *   Limits: T <= 65536 (larger T returns MOE_ERR_UNSUPPORTED), n_routed <= 256, n_groups <= 32.
+ *   All calls share that array: calls that overlap on the GPU race and give wrong results.
+ *   Nothing in it needs clearing between calls (each call writes what it reads).
+ *   The first call on a device looks up the array's device address (once per device, with
+ *   that device current); make it before any stream capture. No allocation happens, ever.
+ */
+moe_status moe_permute_static_scratch(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
+                                      const float* topk_w, const void* x, int32_t* offsets,
+                                      int32_t* row_token, int32_t* slot_row, void* x_perm,
+                                      moe_stream_t stream);
+
+/*
  * Routed + shared SwiGLU experts ([P3] DeepSeek-v1, [P2] sections 2.1-2.2):
  *   for every row r of expert e's segment: h = silu(x_perm[r] W13_e[0:I]^T) * (x_perm[r] W13_e[I:2I]^T),
  *   y_perm[r] = h W2_e^T;  y_shared[t] = sum over shared experts s of the same on x[t].

@@ -15,7 +15,7 @@ __all__ = ["MoeError", "MoeConfig", "MoeWeights", "lib", "make_config", "make_we
            "moe_workspace_size", "moe_route", "moe_load_stats", "moe_permute",
            "moe_expert_ffn", "moe_expert_up", "moe_expert_down", "moe_combine",
            "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
-           "moe_status_string", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
+           "moe_status_string", "moe_permute_static_scratch", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
            "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT",
            "MOE_ERR_DEVICE_CHECK"]
 
@@ -29,7 +29,7 @@ MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_load_stats", "moe_permute",
                     "moe_expert_ffn", "moe_expert_up", "moe_expert_down", "moe_combine",
                     "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
-                    "moe_status_string", "moe_last_error_detail")
+                    "moe_status_string", "moe_last_error_detail", "moe_permute_static_scratch")
 
 
 class MoeError(RuntimeError):
@@ -67,6 +67,7 @@ def _load():
         "moe_route": (I32, [CFG, I32, P, W, P, P, P, P, P, SZ, P]),
         "moe_load_stats": (I32, [CFG, I32, P, P, P, P, P, P, P, SZ, P]),
         "moe_permute": (I32, [CFG, I32, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_permute_static_scratch": (I32, [CFG, I32, P, P, P, P, P, P, P, P]),
         "moe_expert_ffn": (I32, [CFG, I32, P, P, P, W, P, P, P, SZ, P]),
         "moe_expert_up": (I32, [CFG, I32, P, P, P, W, P, P, P]),
         "moe_expert_down": (I32, [CFG, I32, P, P, P, W, P, P, P]),
@@ -175,6 +176,16 @@ def moe_permute(cfg, T, topk_idx, topk_w, x, offsets, row_token, slot_row, x_per
     _check(lib.moe_permute(ctypes.byref(_cfg(cfg)), int(T), _ptr(topk_idx), _ptr(topk_w),
                            _ptr(x), _ptr(offsets), _ptr(row_token), _ptr(slot_row),
                            _ptr(x_perm), p, n, _stream(stream)), "moe_permute")
+
+
+def moe_permute_static_scratch(cfg, T, topk_idx, topk_w, x, offsets, row_token, slot_row,
+                               x_perm, stream=None):
+    """moe_permute for callers that cannot allocate: scratch lives in the library's own
+    2.5 MiB device array (T <= 65536; concurrent calls race)."""
+    _check(lib.moe_permute_static_scratch(ctypes.byref(_cfg(cfg)), int(T), _ptr(topk_idx),
+                                          _ptr(topk_w), _ptr(x), _ptr(offsets), _ptr(row_token),
+                                          _ptr(slot_row), _ptr(x_perm), _stream(stream)),
+           "moe_permute_static_scratch")
 
 
 def moe_expert_ffn(cfg, T, x_perm, offsets, x, weights, y_perm, y_shared, ws, stream=None):

@@ -284,6 +284,18 @@ moe_status check_weights(const moe_config* c, const moe_weights* w, bool need_ga
 
 }  // namespace
 
+// Accessors for other entry-point files of this library (same checks, same error reporting).
+namespace moe {
+moe_status abi_check_config(const moe_config* c, int32_t T) {
+  g_detail[0] = 0;
+  return check_cfg(c, T);
+}
+moe_status abi_fail(moe_status s, const char* msg) { return fail(s, "%s", msg); }
+moe_status abi_cuda_status(cudaError_t e, const char* what) { return cuda_status(e, what); }
+int* abi_error_word() { return error_word(); }
+int abi_num_sms() { return num_sms(); }
+}  // namespace moe
+
 // ==================================================================== exported entry points
 extern "C" {
 

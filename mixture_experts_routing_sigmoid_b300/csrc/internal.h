@@ -92,6 +92,16 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st);
 // fp32 on CUDA cores (gemm_simt.cu)
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t st);
 
+// Shared argument checking and error reporting of the C ABI (abi.cu).
+}  // namespace moe
+#include "../../include/moe.h"
+namespace moe {
+moe_status abi_check_config(const moe_config* c, int32_t T);
+moe_status abi_fail(moe_status s, const char* msg);
+moe_status abi_cuda_status(cudaError_t e, const char* what);
+int* abi_error_word();
+int abi_num_sms();
+
 // Self-test of the bounded wait: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(int* err, unsigned long long timeout_ns, cudaStream_t st);
 
