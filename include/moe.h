@@ -209,6 +209,51 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
                              const moe_weights* w, void* out, int32_t* counts, float* lb_z,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/*
+ * Sequence-wise balance loss ([P3] DeepSeek-v3, "sequence粒度的负载均衡loss"): the expert-level
+ * balance loss of moe_load_stats computed within each sequence instead of over the batch, and
+ * averaged over the sequences. The page gives no formula; this is the plain reading:
+ *   L_b = N sum_e f_e^b P_e^b with f_e^b = (assignments of sequence b to e) / (seq_len K) and
+ *   P_e^b = (sum of e's scores over b's tokens) / (sum of all scores over b's tokens);
+ *   loss = (1/B) sum_b L_b over the B = T / seq_len sequences of seq_len consecutive tokens.
+ * It equals 1 when routing is uniform inside every sequence and N / K when every sequence
+ * collapses onto K experts, even if the batch as a whole is balanced.
+ *   logits [T, N] fp32 and topk_idx [T, K] int32 (from moe_route); per_seq [T / seq_len] fp32
+ *   out or NULL; loss [1] fp32 out. seq_len must divide T.
+ */
+moe_status moe_seq_balance_loss(const moe_config* cfg, int32_t T, int32_t seq_len,
+                                const float* logits, const int32_t* topk_idx, float* per_seq,
+                                float* loss, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Auxiliary-loss-free balancing bias update ([P3] DeepSeek-v3, "Auxiliary-Loss-Free load
+ * balancing"): after a batch, each expert's selection bias moves by `rate` against its load:
+ *   e_i = mean_j counts[j] - counts[i];  select_bias[i] += rate * sign(e_i)
+ * (overloaded experts lose rate, underloaded ones gain it, an expert exactly at the mean keeps
+ * its bias). The sign is decided exactly in integers; the addition is one fp32 add.
+ *   counts [N] int32 (from moe_load_stats or moe_layer_forward), select_bias [N] fp32 in/out,
+ *   rate >= 0 (the page's bias update rate u).
+ */
+moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float rate,
+                           float* select_bias, moe_stream_t stream);
+
+/*
+ * Optional per-stage timing of moe_layer_forward (measurement aid; not thread-safe, one host
+ * thread). Between start and stop, each of the first `max_calls` moe_layer_forward calls of
+ * this process records a CUDA event on its stream at the start of every stage and at its end;
+ * nothing synchronises inside the calls. Stages, in order:
+ *   0 gate GEMM, 1 routing, 2 load statistics (zero when not requested), 3 permutation
+ *   (drop thresholds, histogram, scan, scatter), 4 row dispatch (x -> x_perm), 5 expert up
+ *   GEMM (routed + shared, SwiGLU), 6 expert down GEMM, 7 combine.
+ * moe_stage_timing_start creates the events (host resources only, no device memory).
+ * moe_stage_timing_stop waits for the recorded events, writes the summed milliseconds of the
+ * first n_stages stages over the recorded calls to stage_ms (may be NULL), the number of
+ * recorded calls to *calls (may be NULL), and destroys the events.
+ */
+#define MOE_N_STAGES 8
+moe_status moe_stage_timing_start(int32_t max_calls);
+moe_status moe_stage_timing_stop(float* stage_ms, int32_t n_stages, int32_t* calls);
+
 /* Synchronises `stream`, then returns and clears the current device's error word
  * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK), or MOE_ERR_CUDA if the sync failed. */
 moe_status moe_get_error(moe_stream_t stream);

@@ -15,7 +15,8 @@ __all__ = ["MoeError", "MoeConfig", "MoeWeights", "lib", "make_config", "make_we
            "moe_workspace_size", "moe_route", "moe_load_stats", "moe_permute",
            "moe_expert_ffn", "moe_expert_up", "moe_expert_down", "moe_combine",
            "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
-           "moe_status_string", "moe_permute_static_scratch", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
+           "moe_status_string", "moe_permute_static_scratch", "moe_stage_timing_start",
+           "moe_stage_timing_stop", "moe_bias_update", "moe_seq_balance_loss", "STAGE_NAMES", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
            "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT",
            "MOE_ERR_DEVICE_CHECK"]
 
@@ -29,7 +30,12 @@ MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_load_stats", "moe_permute",
                     "moe_expert_ffn", "moe_expert_up", "moe_expert_down", "moe_combine",
                     "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
-                    "moe_status_string", "moe_last_error_detail", "moe_permute_static_scratch")
+                    "moe_status_string", "moe_last_error_detail", "moe_permute_static_scratch",
+                    "moe_stage_timing_start", "moe_stage_timing_stop", "moe_bias_update",
+                    "moe_seq_balance_loss")
+
+# Stages of moe_layer_forward as moe_stage_timing_stop reports them (MOE_N_STAGES).
+STAGE_NAMES = ("gate", "route", "stats", "permute", "dispatch", "up", "down", "combine")
 
 
 class MoeError(RuntimeError):
@@ -77,6 +83,10 @@ def _load():
         "moe_selftest_wait_timeout": (I32, [I32, P]),
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_last_error_detail": (ctypes.c_char_p, []),
+        "moe_stage_timing_start": (I32, [I32]),
+        "moe_bias_update": (I32, [CFG, P, ctypes.c_float, P, P]),
+        "moe_seq_balance_loss": (I32, [CFG, I32, I32, P, P, P, P, P, SZ, P]),
+        "moe_stage_timing_stop": (I32, [P, I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -228,3 +238,28 @@ def moe_get_error(stream=None) -> int:
 def moe_selftest_wait_timeout(timeout_us: int, stream=None):
     _check(lib.moe_selftest_wait_timeout(int(timeout_us), _stream(stream)),
            "moe_selftest_wait_timeout")
+
+
+def moe_stage_timing_start(max_calls: int):
+    _check(lib.moe_stage_timing_start(int(max_calls)), "moe_stage_timing_start")
+
+
+def moe_stage_timing_stop() -> tuple[dict, int]:
+    """-> ({stage name: summed ms over the recorded calls}, number of recorded calls)."""
+    ms = (ctypes.c_float * len(STAGE_NAMES))()
+    calls = ctypes.c_int32(0)
+    _check(lib.moe_stage_timing_stop(ms, len(STAGE_NAMES), ctypes.byref(calls)),
+           "moe_stage_timing_stop")
+    return dict(zip(STAGE_NAMES, [float(v) for v in ms])), int(calls.value)
+
+
+def moe_bias_update(cfg, counts, rate: float, select_bias, stream=None):
+    _check(lib.moe_bias_update(ctypes.byref(_cfg(cfg)), _ptr(counts), float(rate),
+                               _ptr(select_bias), _stream(stream)), "moe_bias_update")
+
+
+def moe_seq_balance_loss(cfg, T, seq_len, logits, topk_idx, per_seq, loss, ws, stream=None):
+    p, n = _ws(ws)
+    _check(lib.moe_seq_balance_loss(ctypes.byref(_cfg(cfg)), int(T), int(seq_len), _ptr(logits),
+                                    _ptr(topk_idx), _ptr(per_seq), _ptr(loss), p, n,
+                                    _stream(stream)), "moe_seq_balance_loss")

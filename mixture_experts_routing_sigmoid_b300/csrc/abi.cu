@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <new>
 
 #include "../../include/moe.h"
 #include "common.cuh"
@@ -101,7 +102,7 @@ size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 // Workspace carve for one config and token count. Every region is 256-byte aligned.
 struct Layout {
   size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_lse,
-      counts, xy_perm, h, h_sh, y_sh, total;
+      counts, seq_s, seq_c, seq_lb, xy_perm, h, h_sh, y_sh, total;
 };
 
 Layout layout(const moe_config* c, int32_t T) {
@@ -127,6 +128,11 @@ Layout layout(const moe_config* c, int32_t T) {
   L.part_s = take(nbs * N * 4);
   L.part_lse = take(nbs * 2 * 8);
   L.counts = take(N * 4);
+  // sequence-wise loss: B * chunks <= T / 64 + B <= T + T / 64 partial rows for any seq_len
+  const size_t seq_rows = Tt + Tt / 64 + 1;
+  L.seq_s = take(seq_rows * N * 4);
+  L.seq_c = take(seq_rows * N * 4);
+  L.seq_lb = take(Tt * 8);
   L.xy_perm = take(A * H * eb);   // x_perm, then reused for y_perm
   L.h = take(A * I * eb);
   L.h_sh = take(Tt * (S > 0 ? S : 1) * I * eb);
@@ -165,6 +171,35 @@ moe_status cuda_status(cudaError_t e, const char* what) {
   } while (0)
 
 cudaStream_t S_(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+#define TRY_S(expr)                       \
+  do {                                    \
+    moe_status _s = (expr);               \
+    if (_s != MOE_OK) return _s;          \
+  } while (0)
+
+// ---------------------------------------------------------------- optional stage timing
+// While active (moe_stage_timing_start .. _stop, one host thread), every moe_layer_forward
+// records a CUDA event on its stream at each stage boundary, so that the time of each stage
+// can be read back per call without synchronising inside the call.
+enum { STAGE_GATE = 0, STAGE_ROUTE, STAGE_STATS, STAGE_PERMUTE, STAGE_DISPATCH, STAGE_UP,
+       STAGE_DOWN, STAGE_COMBINE, N_STAGES };
+static_assert(N_STAGES == MOE_N_STAGES, "stage list of the header");
+
+struct StageTiming {
+  bool on = false;
+  int max_calls = 0;
+  int calls = 0;        // forwards recorded so far
+  int cur = -1;         // call being recorded, -1 = none
+  cudaEvent_t* ev = nullptr;   // [max_calls][N_STAGES + 1]
+};
+StageTiming g_timing;
+
+// Boundary b (the start of stage b; b == N_STAGES is the end of the call) of the current call.
+void stage_mark(int b, cudaStream_t st) {
+  if (!g_timing.on || g_timing.cur < 0) return;
+  cudaEventRecord(g_timing.ev[(size_t)g_timing.cur * (N_STAGES + 1) + b], st);
+}
 
 // ---------------------------------------------------------------- step implementations
 moe_status do_gate(const moe_config* c, int32_t T, const void* x, const moe_weights* w, float* u,
@@ -220,7 +255,9 @@ moe_status do_permute(const moe_config* c, int32_t T, const int32_t* idx, const 
   p.base = at<int32_t>(ws, L.base);
   p.thr = at<unsigned long long>(ws, L.thr);
   p.err = error_word();
-  return cuda_status(launch_permute(p, num_sms(), st), "permute");
+  TRY_S(cuda_status(launch_permute(p, num_sms(), st), "permute"));
+  stage_mark(STAGE_DISPATCH, st);
+  return cuda_status(launch_dispatch(p, num_sms(), st), "row dispatch");
 }
 
 moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32_t* offsets,
@@ -281,6 +318,38 @@ moe_status check_weights(const moe_config* c, const moe_weights* w, bool need_ga
     moe_status _s = (expr);               \
     if (_s != MOE_OK) return _s;          \
   } while (0)
+
+// The whole layer on `st`, intermediates carved from `ws` (arguments already checked).
+moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const moe_weights* w,
+                       void* out, int32_t* counts, float* lb_z, void* ws, cudaStream_t st) {
+  const Layout L = layout(cfg, T);
+  float* u = at<float>(ws, L.u);
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* wt = at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* slot_row = at<int32_t>(ws, L.slot_row);
+  int32_t* row_token = at<int32_t>(ws, L.row_token);
+  void* xy = at<char>(ws, L.xy_perm);
+  void* h = at<char>(ws, L.h);
+  void* h_sh = cfg->n_shared > 0 ? at<char>(ws, L.h_sh) : nullptr;
+  void* y_sh = cfg->n_shared > 0 ? at<char>(ws, L.y_sh) : nullptr;
+
+  stage_mark(STAGE_GATE, st);
+  TRY(do_gate(cfg, T, x, w, u, st));
+  stage_mark(STAGE_ROUTE, st);
+  TRY(do_route(cfg, T, u, w, idx, wt, st));
+  stage_mark(STAGE_STATS, st);
+  if (counts != nullptr || lb_z != nullptr)
+    TRY(do_stats(cfg, T, u, idx, counts, nullptr, nullptr, lb_z, ws, st));
+  stage_mark(STAGE_PERMUTE, st);
+  TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, slot_row, xy, ws, st));
+  stage_mark(STAGE_UP, st);
+  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, st));
+  stage_mark(STAGE_DOWN, st);
+  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, st));  // y_perm overwrites x_perm
+  stage_mark(STAGE_COMBINE, st);
+  return do_combine(cfg, T, xy, slot_row, wt, y_sh, out, st);
+}
 
 }  // namespace
 
@@ -450,27 +519,110 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   CHECK_ALIGN(lb_z);
   TRY(check_weights(cfg, w, true, true));
   TRY(check_ws(cfg, T, ws, ws_bytes));
-  const Layout L = layout(cfg, T);
-  cudaStream_t st = S_(stream);
-  float* u = at<float>(ws, L.u);
-  int32_t* idx = at<int32_t>(ws, L.idx);
-  float* wt = at<float>(ws, L.w);
-  int32_t* offsets = at<int32_t>(ws, L.offsets);
-  int32_t* slot_row = at<int32_t>(ws, L.slot_row);
-  int32_t* row_token = at<int32_t>(ws, L.row_token);
-  void* xy = at<char>(ws, L.xy_perm);
-  void* h = at<char>(ws, L.h);
-  void* h_sh = cfg->n_shared > 0 ? at<char>(ws, L.h_sh) : nullptr;
-  void* y_sh = cfg->n_shared > 0 ? at<char>(ws, L.y_sh) : nullptr;
+  const bool timed = g_timing.on && g_timing.calls < g_timing.max_calls;
+  if (timed) g_timing.cur = g_timing.calls++;
+  const moe_status s = layer_steps(cfg, T, x, w, out, counts, lb_z, ws, S_(stream));
+  if (timed) {
+    stage_mark(N_STAGES, S_(stream));
+    g_timing.cur = -1;
+  }
+  return s;
+}
 
-  TRY(do_gate(cfg, T, x, w, u, st));
-  TRY(do_route(cfg, T, u, w, idx, wt, st));
-  if (counts != nullptr || lb_z != nullptr)
-    TRY(do_stats(cfg, T, u, idx, counts, nullptr, nullptr, lb_z, ws, st));
-  TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, slot_row, xy, ws, st));
-  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, st));
-  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, st));  // y_perm overwrites x_perm
-  return do_combine(cfg, T, xy, slot_row, wt, y_sh, out, st);
+moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float rate,
+                           float* select_bias, moe_stream_t stream) {
+  g_detail[0] = 0;
+  TRY(check_cfg(cfg, 0));
+  CHECK_PTR(counts);
+  CHECK_PTR(select_bias);
+  if (!std::isfinite(rate) || rate < 0.0f)
+    return fail(MOE_ERR_INVALID_ARG, "rate must be finite and >= 0");
+  BiasUpdateArgs a;
+  a.N = cfg->n_routed;
+  a.counts = counts;
+  a.rate = rate;
+  a.bias = select_bias;
+  return cuda_status(launch_bias_update(a, S_(stream)), "bias update");
+}
+
+moe_status moe_seq_balance_loss(const moe_config* cfg, int32_t T, int32_t seq_len,
+                                const float* logits, const int32_t* topk_idx, float* per_seq,
+                                float* loss, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  g_detail[0] = 0;
+  TRY(check_cfg(cfg, T));
+  if (T == 0) return fail(MOE_ERR_INVALID_ARG, "the sequence loss needs T > 0");
+  if (seq_len < 1 || T % seq_len != 0)
+    return fail(MOE_ERR_INVALID_ARG, "seq_len=%d must divide T=%d", seq_len, T);
+  CHECK_PTR(logits);
+  CHECK_PTR(topk_idx);
+  CHECK_ALIGN(per_seq);
+  CHECK_PTR(loss);
+  TRY(check_ws(cfg, T, ws, ws_bytes));
+  const Layout L = layout(cfg, T);
+  SeqLossArgs a;
+  a.T = T; a.N = cfg->n_routed; a.K = cfg->top_k; a.L = seq_len; a.B = T / seq_len;
+  a.cps = seq_loss_chunks(seq_len);
+  a.score_fn = cfg->score_fn;
+  a.u = logits; a.idx = topk_idx;
+  a.part_s = at<float>(ws, L.seq_s);
+  a.part_c = at<int32_t>(ws, L.seq_c);
+  a.seq_lb = at<double>(ws, L.seq_lb);
+  a.per_seq = per_seq; a.mean = loss;
+  a.err = error_word();
+  return cuda_status(launch_seq_loss(a, S_(stream)), "sequence balance loss");
+}
+
+moe_status moe_stage_timing_start(int32_t max_calls) {
+  g_detail[0] = 0;
+  if (max_calls < 1 || max_calls > 100000)
+    return fail(MOE_ERR_INVALID_ARG, "max_calls=%d not in [1, 100000]", max_calls);
+  if (g_timing.on) return fail(MOE_ERR_INVALID_ARG, "stage timing already active");
+  const size_t n = (size_t)max_calls * (N_STAGES + 1);
+  cudaEvent_t* ev = new (std::nothrow) cudaEvent_t[n];
+  if (ev == nullptr) return fail(MOE_ERR_INVALID_ARG, "host memory for %zu events", n);
+  for (size_t i = 0; i < n; ++i) {
+    const cudaError_t e = cudaEventCreate(&ev[i]);
+    if (e != cudaSuccess) {
+      for (size_t j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      delete[] ev;
+      return cuda_status(e, "cudaEventCreate");
+    }
+  }
+  g_timing.ev = ev;
+  g_timing.max_calls = max_calls;
+  g_timing.calls = 0;
+  g_timing.cur = -1;
+  g_timing.on = true;
+  return MOE_OK;
+}
+
+moe_status moe_stage_timing_stop(float* stage_ms, int32_t n_stages, int32_t* calls) {
+  g_detail[0] = 0;
+  if (!g_timing.on) return fail(MOE_ERR_INVALID_ARG, "stage timing not active");
+  moe_status st = MOE_OK;
+  if (stage_ms != nullptr && (n_stages < 0 || n_stages > N_STAGES))
+    st = fail(MOE_ERR_INVALID_ARG, "n_stages=%d not in [0, %d]", n_stages, N_STAGES);
+  const int nc = g_timing.calls;
+  if (st == MOE_OK && stage_ms != nullptr) {
+    for (int b = 0; b < n_stages; ++b) stage_ms[b] = 0.0f;
+    for (int c = 0; c < nc && st == MOE_OK; ++c) {
+      cudaEvent_t* e = g_timing.ev + (size_t)c * (N_STAGES + 1);
+      cudaError_t ce = cudaEventSynchronize(e[N_STAGES]);
+      if (ce != cudaSuccess) { st = cuda_status(ce, "cudaEventSynchronize"); break; }
+      for (int b = 0; b < n_stages; ++b) {
+        float ms = 0.0f;
+        ce = cudaEventElapsedTime(&ms, e[b], e[b + 1]);
+        if (ce != cudaSuccess) { st = cuda_status(ce, "cudaEventElapsedTime"); break; }
+        stage_ms[b] += ms;
+      }
+    }
+  }
+  if (calls != nullptr) *calls = nc;
+  const size_t n = (size_t)g_timing.max_calls * (N_STAGES + 1);
+  for (size_t i = 0; i < n; ++i) cudaEventDestroy(g_timing.ev[i]);
+  delete[] g_timing.ev;
+  g_timing = StageTiming();
+  return st;
 }
 
 moe_status moe_get_error(moe_stream_t stream) {

@@ -9,18 +9,39 @@
 // stacked into one of intermediate size S*I ("DeepSeek MoE：从v1到v3的演进", DeepSeek-v1
 // fine-grained experts and shared-expert isolation).
 //
-// Persistent kernel, one 192-thread CTA per SM, static round-robin over output tiles of
-// 128 rows x 256 columns (UP: 128 gate + 128 up columns of the same 128 intermediate
-// features, so the SwiGLU is applied in the epilogue). Tiles run problem by problem, weight
-// tile by weight tile, row tile fastest, so CTAs that run together share weight tiles in L2.
-//   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage, 128-byte
-//               swizzle, 4-stage ring of 48 KB stages guarded by full/empty mbarriers.
-//   warp 1      TMEM owner and MMA issuer: one thread issues 4 tcgen05.mma (M=128, N=256,
-//               K=16) per stage into one of two 256-column fp32 accumulators, commits the
-//               stage back to the producer and the finished accumulator to the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//               32*(w%4)..+31 = tile rows), SwiGLU / bias, row-predicated 16-byte stores.
-// Rows of a tile past the segment end belong to the next expert (or lie beyond the tensor,
+// Weight rows are the MMA's M side and tokens its N side ("swap AB"), and each tile runs on a
+// pair of SMs (a cluster of two CTAs issuing tcgen05.mma.cta_group::2): D[w_row, token] =
+// sum_k W[w_row, k] A[token, k]. Each CTA loads its own 128 weight rows and half of the tile's
+// tokens; the pair's first CTA issues the MMA, which reads both CTAs' shared memory and writes
+// each CTA's 128 rows of D into that CTA's TMEM. The instruction's N can be any multiple of
+// 16, so a segment's ragged end costs at most 15 idle token columns instead of a mostly empty
+// row tile, and in decode (a few tokens per expert) the weights stream through at full width
+// while the token operand stays tiny.
+//   UP:   per CTA, 64 intermediate features: its 128 weight rows interleave the gate and up
+//         projections 16 rows at a time (rows 32q..32q+15 gate rows of features 16q..16q+15,
+//         rows 32q+16..32q+31 the up rows of the same features; one 5-D TMA box loads them),
+//         so warp q of the epilogue holds both halves of its 16 features and pairs them with
+//         one shuffle before applying the SwiGLU in registers.
+//   DOWN: 128 output features per CTA, up to 256 tokens per tile.
+//   GATE: 128 router outputs per CTA (rows past n_routed read as zero), up to 256 tokens.
+// A TMEM lane is one output feature and a column one token, so after tcgen05.ld a warp holds
+// 32 consecutive features of each of 32 tokens: the epilogue stores straight from registers,
+// each store instruction covering a contiguous run of one token's output row (neighbouring
+// lanes swap values to write bf16 pairs). No shared-memory staging.
+//
+// Persistent kernel, one 192-thread CTA per SM, CTA pairs take tiles round-robin in the order
+// problem by problem, weight tile by weight tile, token tile fastest (a segment's rows are
+// split into equal token tiles), so the pairs running together share weight tiles in L2.
+//   warp 0      TMA producer (both CTAs): this CTA's weight rows and token rows of one k block
+//               (64 elements) per stage, 128-byte swizzle, 6-stage ring of 32 KB stages.
+//               Completion of both CTAs' loads is counted on the first CTA's full barrier; the
+//               MMA's commit frees the stage in both CTAs.
+//   warp 1      TMEM owner (both CTAs) and, in the first CTA, MMA issuer: a single thread waits
+//               for each stage and issues its four tcgen05.mma (M=256, N=tile's tokens rounded
+//               up to 16, K=16) into one of two 256-column fp32 accumulators.
+//   warps 2..5  epilogue (both CTAs): tcgen05.ld of the warp's 32 TMEM lanes, SwiGLU / router
+//               bias, stores.
+// Token columns past the segment end belong to the next expert (or lie beyond the tensor,
 // where TMA fills zeros); they are computed and never stored. Every mbarrier wait is bounded:
 // on timeout the CTA raises an abort flag and the device error word, drains, frees TMEM and
 // returns.
@@ -33,19 +54,26 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128;                  // weight rows per CTA and operand (MMA M = 256)
+constexpr int BK = 64;                   // reduction elements per stage (128 bytes of bf16)
 constexpr int MAXP = 258;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr uint32_t ACC_COLS = 256;       // two accumulators
+constexpr int XBOX_S = 32, XBOX_L = 64;  // token rows per TMA box (small / large map)
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;    // 2 s per wait
 constexpr unsigned long long GRACE_NS = 100000000ull;       // drain after an abort
 
+constexpr int TOK = 256;                 // tokens per tile at most (MMA N)
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;     // this CTA's weight rows
+constexpr int B_BYTES = TOK / 2 * BK * 2;  // this CTA's token rows (at most)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+
 struct TcParams {
-  CUtensorMap tmA0, tmA1, tmB0, tmB1;
+  CUtensorMap tmW0, tmW1;    // weights: routed, shared (box 128 rows; UP: interleaved 5-D box)
+  CUtensorMap tmX0, tmX1;    // tokens: routed, shared (box 64 rows)
+  CUtensorMap tmX0s, tmX1s;  // tokens: routed, shared (box 32 rows)
   const int32_t* offsets;
   int n_routed, has_shared, T, H, I, S, N;
   void* out0;
@@ -55,10 +83,10 @@ struct TcParams {
 };
 
 struct SmemCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[STAGES];       // first CTA's copy counts both CTAs' loads
+  uint64_t empty[STAGES];      // per CTA, arrived on by the MMA commit
+  uint64_t tfull[2];           // per CTA, arrived on by the MMA commit
+  uint64_t tempty[2];          // first CTA's copy: 4 epilogue warps x 2 CTAs
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -70,12 +98,21 @@ struct SmemCtl {
 };
 
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 template <int MODE>
-__device__ __forceinline__ int n_tiles_of(const TcParams& p, bool shared) {
-  if (MODE == MODE_UP) return (shared ? p.S * p.I : p.I) / 128;
-  if (MODE == MODE_DOWN) return (p.H + BN - 1) / BN;
-  return 1;
+__device__ __forceinline__ int feat_total(const TcParams& p, bool shared) {
+  if (MODE == MODE_UP) return shared ? p.S * p.I : p.I;
+  if (MODE == MODE_DOWN) return p.H;
+  return p.N;
+}
+// Output features of one CTA: UP 64 (gate and up rows of each), else 128.
+template <int MODE>
+__host__ __device__ constexpr int feat_per_cta() { return MODE == MODE_UP ? BM / 2 : BM; }
+// Feature tiles of 2 * feat_per_cta outputs.
+template <int MODE>
+__device__ __forceinline__ int n_feat_tiles(const TcParams& p, bool shared) {
+  return (feat_total<MODE>(p, shared) + 2 * feat_per_cta<MODE>() - 1) / (2 * feat_per_cta<MODE>());
 }
 template <int MODE>
 __device__ __forceinline__ int k_blocks_of(const TcParams& p, bool shared) {
@@ -84,7 +121,14 @@ __device__ __forceinline__ int k_blocks_of(const TcParams& p, bool shared) {
 }
 
 struct Tile {
-  int prob, m0, n0, row0, rows, kb;
+  int prob;      // problem index
+  int f0;        // first output feature of the tile; this CTA's are f0 + feat_per_cta * rank ..
+  int r0;        // first token row (in the problem's activation tensor)
+  int nrows;     // token rows of this tile that are stored
+  int ncols;     // MMA N: nrows rounded up to 16; each CTA holds ncols / 2 token rows
+  int nbox;      // token boxes loaded per CTA and stage
+  bool big_box;  // boxes of 64 rows (else one box of 32)
+  int kb;        // k blocks
   bool shared;
 };
 
@@ -98,16 +142,67 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   Tile t;
   t.prob = lo;
   t.shared = (MODE != MODE_GATE) && lo >= p.n_routed;
-  t.row0 = c.row0[lo];
-  t.rows = c.rows[lo];
-  const int mt = (t.rows + BM - 1) / BM;
+  const int rows = c.rows[lo];
+  const int ntt = (rows + TOK - 1) / TOK;
   const int local = tile - c.tile_start[lo];
-  const int n = local / mt;
-  const int m = local - n * mt;
-  t.m0 = m * BM;
-  t.n0 = (MODE == MODE_UP) ? n * 128 : n * BN;
+  const int ft = local / ntt;
+  const int tt = local - ft * ntt;
+  t.f0 = ft * 2 * feat_per_cta<MODE>();
+  // a segment's rows split into ntt token tiles of equal size (a multiple of 16)
+  const int per = (((rows + ntt - 1) / ntt) + 15) & ~15;
+  t.r0 = c.row0[lo] + tt * per;
+  t.nrows = min(per, rows - tt * per);
+  t.ncols = (t.nrows + 15) & ~15;
+  const int half = t.ncols / 2;
+  t.big_box = half > XBOX_S;
+  t.nbox = t.big_box ? (half + XBOX_L - 1) / XBOX_L : 1;
   t.kb = k_blocks_of<MODE>(p, t.shared);
   return t;
+}
+
+// Coordinates of this CTA's boxes for k block kb of tile t: the weight box at (ax, ay0) (UP:
+// 5-D coordinates (ax, 0, 0, ay0 = first 16-feature group, ay1 = expert)); token boxes at
+// (bx, by0 + box_rows j), j < t.nbox.
+struct Boxes {
+  const CUtensorMap* tw;
+  const CUtensorMap* tx;
+  int ax, ay0, ay1, bx, by0, box_rows, box_bytes;
+};
+
+template <int MODE>
+__device__ __forceinline__ Boxes boxes_of(const TcParams& p, const Tile& t, int kb, uint32_t rank) {
+  Boxes b;
+  b.tw = t.shared ? &p.tmW1 : &p.tmW0;
+  if (t.big_box) {
+    b.tx = t.shared ? &p.tmX1 : &p.tmX0;
+    b.box_rows = XBOX_L;
+  } else {
+    b.tx = t.shared ? &p.tmX1s : &p.tmX0s;
+    b.box_rows = XBOX_S;
+  }
+  b.box_bytes = b.box_rows * BK * 2;
+  const int k0 = kb * BK;
+  b.ax = k0;
+  b.ay1 = 0;
+  int fc = t.f0 + (int)rank * feat_per_cta<MODE>();    // this CTA's first feature
+  if (fc >= feat_total<MODE>(p, t.shared)) fc = t.f0;  // past the end: recompute CTA 0's rows
+  if (MODE == MODE_UP) {
+    const int s = fc / p.I, j = fc - s * p.I;          // expert (shared: stacked), feature in it
+    b.ay0 = j / 16;
+    b.ay1 = t.shared ? s : t.prob;
+  } else if (MODE == MODE_DOWN) {
+    if (!t.shared) {
+      b.ay0 = t.prob * p.H + fc;
+    } else {
+      b.ax = k0 % p.I;
+      b.ay0 = (k0 / p.I) * p.H + fc;
+    }
+  } else {
+    b.ay0 = fc;
+  }
+  b.bx = k0;
+  b.by0 = t.r0 + (int)rank * (t.ncols / 2);
+  return b;
 }
 
 __device__ __forceinline__ void grace_wait(uint32_t bar, uint32_t parity) {
@@ -116,8 +211,34 @@ __device__ __forceinline__ void grace_wait(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > GRACE_NS) break;
 }
 
+__device__ __forceinline__ void grace_sleep() {
+  const unsigned long long t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < GRACE_NS / 10) {
+  }
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.0f + __expf(-g)) * u;
+}
+
+// Stores this lane's feature f (f of lanes l and l^1 differ in the last bit) for tokens
+// row0 .. row0 + NT - 1 of a row-major bf16 output with leading dimension ld: lanes l and l^1
+// swap one value per token pair so that the even lane writes features (f, f+1) of the even
+// token and the odd lane features (f-1, f) of the odd token, 4 bytes each.
+template <int NT>
+__device__ __forceinline__ void store_bf16_chunk(const float (&v)[NT], __nv_bfloat16* out,
+                                                 size_t ld, size_t row0, int nvalid, int f,
+                                                 bool fvalid, int lane) {
+  const bool odd = lane & 1;
+  __nv_bfloat16* base = out + row0 * ld + (odd ? f - 1 : f);
+#pragma unroll
+  for (int i = 0; i < NT; i += 2) {
+    const float mine = odd ? v[i] : v[i + 1];
+    const float other = __shfl_xor_sync(FULL_MASK, mine, 1);
+    const int tok = odd ? i + 1 : i;
+    const uint32_t pk = odd ? pack_bf16x2(other, v[i + 1]) : pack_bf16x2(v[i], other);
+    if (fvalid && tok < nvalid) *reinterpret_cast<uint32_t*>(base + (size_t)tok * ld) = pk;
+  }
 }
 
 template <int MODE>
@@ -128,17 +249,19 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   uint8_t* sgen = smem_raw + (sbase - raw);
   SmemCtl& c = *reinterpret_cast<SmemCtl*>(sgen + (size_t)STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: issues the MMA; 1: its peer
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   auto bar = [](const uint64_t& b) { return smem_u32(&b); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(bar(c.full[s]), 1); mbar_init(bar(c.empty[s]), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(bar(c.tfull[a]), 1); mbar_init(bar(c.tempty[a]), 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(bar(c.tfull[a]), 1); mbar_init(bar(c.tempty[a]), 8); }
     mbar_init(bar(c.drain), 1);
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(smem_u32(&c.tmem_base), TMEM_COLS);
 
   // ---- problem table and tile prefix (tile counts depend on device-resident offsets)
   const int nprob = (MODE == MODE_GATE) ? 1 : p.n_routed + p.has_shared;
@@ -161,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       if (q < nprob) {
         const bool sh = (MODE != MODE_GATE) && q >= p.n_routed;
         const int rows = c.rows[q] > 0 ? c.rows[q] : 0;
-        cnt = ((rows + BM - 1) / BM) * n_tiles_of<MODE>(p, sh);
+        cnt = ((rows + TOK - 1) / TOK) * n_feat_tiles<MODE>(p, sh);
       }
       int incl = cnt;
 #pragma unroll
@@ -174,8 +297,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     }
     if (lane == 0) { c.tile_start[nprob] = run; c.total_tiles = run; c.nprob = nprob; }
   }
+  // both CTAs' barriers are initialised before either CTA signals the other's
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = c.tmem_base;
   const int total = c.total_tiles;
@@ -184,41 +309,37 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&p.tmA0);
-      tma_prefetch_desc(&p.tmB0);
-      if (MODE != MODE_GATE && p.has_shared) { tma_prefetch_desc(&p.tmA1); tma_prefetch_desc(&p.tmB1); }
+      tma_prefetch_desc(&p.tmW0);
+      tma_prefetch_desc(&p.tmX0);
+      tma_prefetch_desc(&p.tmX0s);
+      if (MODE != MODE_GATE && p.has_shared) {
+        tma_prefetch_desc(&p.tmW1);
+        tma_prefetch_desc(&p.tmX1);
+        tma_prefetch_desc(&p.tmX1s);
+      }
     }
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once / its parity
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = pair; tile < total && ok; tile += npairs) {
       const Tile t = decode_tile<MODE>(p, c, tile);
       for (int kb = 0; kb < t.kb; ++kb) {
         if (!warp_wait_bounded(bar(c.empty[stage]), phase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
           ok = false;
           break;
         }
+        const uint32_t fb = mapa_shared(bar(c.full[stage]), 0);  // the first CTA's barrier
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        const Boxes b = boxes_of<MODE>(p, t, kb, rank);
         if (lane == 0) {
-          const uint32_t fb = bar(c.full[stage]);
-          mbar_expect_tx(fb, STAGE_BYTES);
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          const int k0 = kb * BK;
-          tma_load_2d(sa, t.shared ? &p.tmA1 : &p.tmA0, fb, k0, t.row0 + t.m0);
-          if (MODE == MODE_UP) {
-            int yg;
-            if (!t.shared) yg = t.prob * 2 * p.I + t.n0;
-            else yg = (t.n0 / p.I) * 2 * p.I + (t.n0 % p.I);
-            const CUtensorMap* tb = t.shared ? &p.tmB1 : &p.tmB0;
-            tma_load_2d(sb, tb, fb, k0, yg);                  // gate projection rows
-            tma_load_2d(sb + B_BYTES / 2, tb, fb, k0, yg + p.I);  // up projection rows
-          } else if (MODE == MODE_DOWN) {
-            if (!t.shared) tma_load_2d(sb, &p.tmB0, fb, k0, t.prob * p.H + t.n0);
-            else tma_load_2d(sb, &p.tmB1, fb, k0 % p.I, (k0 / p.I) * p.H + t.n0);
-          } else {
-            tma_load_2d(sb, &p.tmB0, fb, k0, 0);
-          }
+          if (rank == 0) mbar_expect_tx(bar(c.full[stage]), 2 * (A_BYTES + t.nbox * b.box_bytes));
+          if (MODE == MODE_UP) tma_load_5d_pair(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1);
+          else tma_load_2d_pair(sa, b.tw, fb, b.ax, b.ay0);
         }
+        __syncwarp();
+        if (lane < t.nbox)
+          tma_load_2d_pair(sb + lane * b.box_bytes, b.tx, fb, b.bx, b.by0 + lane * b.box_rows);
         __syncwarp();
         issued_mask |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -226,144 +347,132 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       }
     }
     if (ok) {
-      // tail: wait until the MMA warp has released every stage (all its commits landed)
+      // tail: wait until the MMA has released every stage (all its commits landed)
       for (int i = 0; i < STAGES; ++i) {
         if (!warp_wait_bounded(bar(c.empty[stage]), phase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) break;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     if (*abort_flag && lane == 0) {
-      for (int s = 0; s < STAGES; ++s)
-        if ((issued_mask >> s) & 1u) grace_wait(bar(c.full[s]), (last_parity >> s) & 1u);
+      if (rank == 0) {
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued_mask >> s) & 1u) grace_wait(bar(c.full[s]), (last_parity >> s) & 1u);
+      } else {
+        grace_sleep();  // this CTA's loads complete on the other CTA's barriers
+      }
     }
   } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE>(p, c, tile);
-      if (!warp_wait_bounded(bar(c.tempty[acc]), aphase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < t.kb; ++kb) {
-        if (!warp_wait_bounded(bar(c.full[stage]), phase, abort_flag, p.err, TIMEOUT_NS)) {
+    // ================================================================ MMA issuer (first CTA)
+    if (rank == 0 && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        const Tile t = decode_tile<MODE>(p, c, tile);
+        const uint32_t idesc = idesc_bf16_f32(2 * BM, t.ncols);
+        if (!mbar_wait_bounded(bar(c.tempty[acc]), aphase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+        for (int kb = 0; kb < t.kb; ++kb) {
+          if (!mbar_wait_bounded(bar(c.full[stage]), phase, abort_flag, p.err, TIMEOUT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint64_t ad = sdesc_k_sw128(sa);
           const uint64_t bd = sdesc_k_sw128(sa + A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_f16(d_tmem, ad + 2u * kk, bd + 2u * kk, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(c.empty[stage]));
+            tc_mma_f16_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_pair_mc(bar(c.empty[stage]), 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (!ok) break;
+        tc_commit_pair_mc(bar(c.tfull[acc]), 0x3);
+        acc ^= 1u;
+        if (acc == 0) aphase ^= 1u;
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(bar(c.tfull[acc]));
-      __syncwarp();
-      acc ^= 1u;
-      if (acc == 0) aphase ^= 1u;
-    }
-    if (*abort_flag && lane == 0) {
-      tc_commit(bar(c.drain));  // arrives once every MMA issued above has completed
-      grace_wait(bar(c.drain), 0);
+      if (*abort_flag) {
+        tc_commit_pair_mc(bar(c.drain), 0x1);  // arrives once every MMA issued above completed
+        grace_wait(bar(c.drain), 0);
+      }
     }
   } else {
     // ================================================================ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const uint32_t tempty0 = mapa_shared(bar(c.tempty[0]), 0);
+    const uint32_t tempty1 = mapa_shared(bar(c.tempty[1]), 0);
     uint32_t acc = 0, aphase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = pair; tile < total; tile += npairs) {
       const Tile t = decode_tile<MODE>(p, c, tile);
       if (!warp_wait_bounded(bar(c.tfull[acc]), aphase, abort_flag, p.err, TIMEOUT_NS)) break;
       tc_fence_after();
-      const int r = q * 32 + lane;
-      const bool row_ok = t.m0 + r < t.rows;
-      const size_t grow = (size_t)(t.row0 + t.m0 + r);
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (MODE == MODE_UP) {
-        const int ld = t.shared ? p.S * p.I : p.I;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(t.shared ? p.out1 : p.out0);
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t g[32], u[32];
-          tmem_ld_32cols(tb + cc * 32, g);
-          tmem_ld_32cols(tb + 128 + cc * 32, u);
-          tmem_wait_ld_fence(g);
-          reg_fence(u);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + grow * ld + t.n0 + cc * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w4[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int j = v * 8 + 2 * i;
-                w4[i] = pack_bf16x2(silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j])),
-                                    silu_mul(__uint_as_float(g[j + 1]), __uint_as_float(u[j + 1])));
-              }
-              dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          }
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
+      const int fc = t.f0 + (int)rank * feat_per_cta<MODE>();  // this CTA's first feature
+      const int nch = (t.nrows + 31) / 32;
+      for (int ch = 0; ch < nch; ++ch) {
+        const int nvalid = t.nrows - ch * 32;
+        const size_t row0 = (size_t)(t.r0 + ch * 32);
+        uint32_t v[32];
+        tmem_ld_32cols(tb + ch * 32, v);
+        tmem_wait_ld_fence(v);
+        if (ch == nch - 1) {
+          // accumulator fully read: hand it back to the MMA issuer before the stores
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
         }
-      } else if (MODE == MODE_DOWN) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(t.shared ? p.out1 : p.out0);
-#pragma unroll 1
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t v32[32];
-          tmem_ld_32cols(tb + cc * 32, v32);
-          tmem_wait_ld_fence(v32);
-          if (row_ok && t.n0 + cc * 32 < p.H) {
-            uint4* dst = reinterpret_cast<uint4*>(out + grow * p.H + t.n0 + cc * 32);
+        if (MODE == MODE_UP) {
+          // lanes 0..15: gate of features fq + lane; lanes 16..31: up of features fq + lane - 16.
+          // Lane l < 16 computes tokens 0..15 with its partner's up values, lane l + 16 tokens
+          // 16..31 with its partner's gate values.
+          const int fq = fc + q * 16;
+          const bool hi = lane >= 16;
+          float hv[16];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w4[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int j = v * 8 + 2 * i;
-                w4[i] = pack_bf16x2(__uint_as_float(v32[j]), __uint_as_float(v32[j + 1]));
-              }
-              dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float send = __uint_as_float(hi ? v[i] : v[16 + i]);
+            const float recv = __shfl_xor_sync(FULL_MASK, send, 16);
+            hv[i] = hi ? silu_mul(recv, __uint_as_float(v[16 + i]))
+                       : silu_mul(__uint_as_float(v[i]), recv);
           }
-        }
-      } else {
-        float* out = static_cast<float*>(p.out0);
-#pragma unroll 1
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t v32[32];
-          tmem_ld_32cols(tb + cc * 32, v32);
-          tmem_wait_ld_fence(v32);
-          if (row_ok) {
+          const int ld = t.shared ? p.S * p.I : p.I;
+          store_bf16_chunk<16>(hv, static_cast<__nv_bfloat16*>(t.shared ? p.out1 : p.out0), ld,
+                               row0 + (hi ? 16 : 0), nvalid - (hi ? 16 : 0), fq + (lane & 15),
+                               fc < feat_total<MODE>(p, t.shared), lane);
+        } else {
+          const int f = fc + q * 32 + lane;                // this thread's feature
+          // (feature counts are even, so lanes l and l^1 agree on validity)
+          const bool fvalid = f < feat_total<MODE>(p, t.shared);
+          if (MODE == MODE_DOWN) {
+            float yv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int col = cc * 32 + i;
-              if (col < p.N)
-                out[grow * p.N + col] =
-                    __uint_as_float(v32[i]) + (p.gate_bias ? p.gate_bias[col] : 0.0f);
-            }
+            for (int i = 0; i < 32; ++i) yv[i] = __uint_as_float(v[i]);
+            store_bf16_chunk<32>(yv, static_cast<__nv_bfloat16*>(t.shared ? p.out1 : p.out0), p.H,
+                                 row0, nvalid, f, fvalid, lane);
+          } else {
+            float* out = static_cast<float*>(p.out0) + row0 * p.N + f;
+            const float bias = (fvalid && p.gate_bias) ? p.gate_bias[f] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (fvalid && i < nvalid) out[(size_t)i * p.N] = __uint_as_float(v[i]) + bias;
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(c.tempty[acc]));
       acc ^= 1u;
       if (acc == 0) aphase ^= 1u;
     }
   }
 
+  // both CTAs are done with each other's shared memory, barriers and TMEM before either frees
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // One CTA waits on an mbarrier that nothing ever arrives on; the bounded wait must give up,
@@ -407,20 +516,61 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// UP weights [E, 2I, H] (E experts; rows 0..I-1 gate, I..2I-1 up) as a 5-D tensor
+// (k, r, which, g, e) = element (e, which * I + 16 g + r, k), box (64, 16, 2, 4, 1): one load
+// brings 64 features' gate and up rows interleaved 16 at a time (gate 16, up 16, ...).
+bool make_up_weight_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t E) {
+  auto fn = encode_fn();
+  if (fn == nullptr || base == nullptr || H == 0 || I == 0 || E == 0 || I % 64 != 0) return false;
+  cuuint64_t dims[5] = {H, 16, 2, I / 16, E};
+  cuuint64_t strides[4] = {H * 2, I * H * 2, 16 * H * 2, 2 * I * H * 2};
+  cuuint32_t box[5] = {64, 16, 2, 4, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token operand [outer, inner] with both box heights.
+bool make_token_maps(CUtensorMap* big, CUtensorMap* small, const void* base, uint64_t inner,
+                     uint64_t outer) {
+  return make_map(big, base, inner, outer, XBOX_L) && make_map(small, base, inner, outer, XBOX_S);
+}
+
 template <int MODE>
 cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
-  static int attr_set_for_device[64] = {0};
+  static int grid_for_device[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set_for_device[dev]) {
+  int grid = (dev >= 0 && dev < 64) ? grid_for_device[dev] : 0;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (grid == 0) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set_for_device[dev] = 1;
+    // persistent grid: as many CTA pairs as can be resident at once (one CTA per SM)
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<MODE>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    grid = 2 * (clusters < num_sms / 2 ? clusters : num_sms / 2);
+    if (dev >= 0 && dev < 64) grid_for_device[dev] = grid;
   }
-  tc_gemm_kernel<MODE><<<num_sms, THREADS, SMEM_BYTES, st>>>(prm);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(grid, 1, 1);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, prm);
 }
 
 }  // namespace
@@ -439,22 +589,22 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   const uint64_t H = a.H, I = a.I, S = a.S, N = a.N, T = a.T, R = a.rows_cap;
   bool ok = true;
   if (a.mode == MODE_GATE) {
-    ok = make_map(&prm.tmA0, a.a0, H, T, 128) && make_map(&prm.tmB0, a.b0, H, N, 256);
+    ok = make_map(&prm.tmW0, a.b0, H, N, BM) && make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, T);
     if (!ok) return cudaErrorInvalidValue;
     return launch_mode<MODE_GATE>(prm, num_sms, st);
   }
   if (a.mode == MODE_UP) {
-    if (a.n_routed > 0) ok = ok && make_map(&prm.tmA0, a.a0, H, R, 128) &&
-                             make_map(&prm.tmB0, a.b0, H, N * 2 * I, 128);
-    if (a.has_shared) ok = ok && make_map(&prm.tmA1, a.a1, H, T, 128) &&
-                           make_map(&prm.tmB1, a.b1, H, S * 2 * I, 128);
+    if (a.n_routed > 0) ok = ok && make_up_weight_map(&prm.tmW0, a.b0, H, I, N) &&
+                             make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, R);
+    if (a.has_shared) ok = ok && make_up_weight_map(&prm.tmW1, a.b1, H, I, S) &&
+                           make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, H, T);
     if (!ok) return cudaErrorInvalidValue;
     return launch_mode<MODE_UP>(prm, num_sms, st);
   }
-  if (a.n_routed > 0) ok = ok && make_map(&prm.tmA0, a.a0, I, R, 128) &&
-                           make_map(&prm.tmB0, a.b0, I, N * H, 256);
-  if (a.has_shared) ok = ok && make_map(&prm.tmA1, a.a1, S * I, T, 128) &&
-                         make_map(&prm.tmB1, a.b1, I, S * H, 256);
+  if (a.n_routed > 0) ok = ok && make_map(&prm.tmW0, a.b0, I, N * H, BM) &&
+                           make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, I, R);
+  if (a.has_shared) ok = ok && make_map(&prm.tmW1, a.b1, I, S * H, BM) &&
+                         make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, S * I, T);
   if (!ok) return cudaErrorInvalidValue;
   return launch_mode<MODE_DOWN>(prm, num_sms, st);
 }

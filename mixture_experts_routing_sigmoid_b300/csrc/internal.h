@@ -35,6 +35,29 @@ struct StatsArgs {
 int stats_blocks(int T);
 cudaError_t launch_stats(const StatsArgs& a, cudaStream_t st);
 
+// ---------------------------------------------------------------- balancing (balance.cu)
+struct BiasUpdateArgs {
+  int N;
+  const int32_t* counts;  // [N]
+  float rate;
+  float* bias;            // [N] in/out
+};
+cudaError_t launch_bias_update(const BiasUpdateArgs& a, cudaStream_t st);
+
+struct SeqLossArgs {
+  int T, N, K, L, B, cps, score_fn;  // B = T / L sequences, cps chunks per sequence
+  const float* u;         // [T, N] logits
+  const int32_t* idx;     // [T, K]
+  float* part_s;          // scratch [B * cps, N]
+  int32_t* part_c;        // scratch [B * cps, N]
+  double* seq_lb;         // scratch [B]
+  float* per_seq;         // [B] or nullptr
+  float* mean;            // [1]
+  int* err;
+};
+int seq_loss_chunks(int L);
+cudaError_t launch_seq_loss(const SeqLossArgs& a, cudaStream_t st);
+
 // ---------------------------------------------------------------- permutation (permute.cu)
 struct PermuteArgs {
   int T, N, K, D, capacity_drop;
@@ -54,7 +77,10 @@ struct PermuteArgs {
   int* err;
 };
 int permute_blocks(int T);
+// drop thresholds, histogram, scan, scatter: offsets, row_token, slot_row
 cudaError_t launch_permute(const PermuteArgs& a, int num_sms, cudaStream_t st);
+// x_perm[slot_row(t,k)] = x[t] (no-op when x or x_perm is null)
+cudaError_t launch_dispatch(const PermuteArgs& a, int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------- combine (combine.cu)
 struct CombineArgs {

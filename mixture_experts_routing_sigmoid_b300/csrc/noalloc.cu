@@ -109,7 +109,10 @@ extern "C" moe_status moe_permute_static_scratch(const moe_config* cfg, int32_t 
   p.base = reinterpret_cast<int32_t*>(base + kMaskBytes + kCountBytes);
   p.thr = reinterpret_cast<unsigned long long*>(base + kMaskBytes + 2 * kCountBytes);
   p.err = moe::abi_error_word();
-  return moe::abi_cuda_status(
-      moe::launch_permute(p, moe::abi_num_sms(), reinterpret_cast<cudaStream_t>(stream)),
-      "permute (static scratch)");
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  st = moe::abi_cuda_status(moe::launch_permute(p, moe::abi_num_sms(), cs),
+                            "permute (static scratch)");
+  if (st != MOE_OK) return st;
+  return moe::abi_cuda_status(moe::launch_dispatch(p, moe::abi_num_sms(), cs),
+                              "row dispatch (static scratch)");
 }

@@ -192,11 +192,14 @@ cudaError_t launch_permute(const PermuteArgs& p, int num_sms, cudaStream_t st) {
   perm_hist_kernel<<<nb, PB, p.N * 8 * sizeof(uint32_t), st>>>(p);
   perm_scan_kernel<<<1, 256, 0, st>>>(p, nb);
   perm_scatter_kernel<<<nb, PB, 0, st>>>(p);
-  if (p.x != nullptr && p.x_perm != nullptr) {
-    int blocks = (p.T + 7) / 8;
-    if (blocks > num_sms * 8) blocks = num_sms * 8;
-    dispatch_rows_kernel<<<blocks, 256, 0, st>>>(p);
-  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const PermuteArgs& p, int num_sms, cudaStream_t st) {
+  if (p.T <= 0 || p.x == nullptr || p.x_perm == nullptr) return cudaSuccess;
+  int blocks = (p.T + 7) / 8;
+  if (blocks > num_sms * 8) blocks = num_sms * 8;
+  dispatch_rows_kernel<<<blocks, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -90,6 +90,11 @@ CONFIGS: dict[str, LayerConfig] = {
     "v3_decode_32": LayerConfig("v3_decode_32", T=32, logit_offset="zipf", **_V3),
     "v3_decode_128": LayerConfig("v3_decode_128", T=128, logit_offset="zipf", **_V3),
     "v3_decode_512": LayerConfig("v3_decode_512", T=512, logit_offset="zipf", **_V3),
+    # Profiling case of the V3 prefill GEMMs: the same shapes and per-expert load (512 rows per
+    # expert on average) with 1/8 of the experts and tokens, so that a detailed profiler
+    # capture holds about 3 GB on the device while its operands still exceed L2.
+    "v3_prefill_e32": LayerConfig("v3_prefill_e32", T=2048, logit_offset="none",
+                                  **{**_V3, "n_routed": 32}),
 }
 
 

@@ -129,6 +129,22 @@ def load_stats(cfg, u, s, idx) -> LoadStats:
     return LoadStats(counts, f, P, float(out3[0]), float(out3[1]), float(out3[2]))
 
 
+def seq_balance_loss(cfg, u, s, idx, seq_len: int):
+    """Sequence-wise balance loss ("DeepSeek MoE：从v1到v3的演进", DeepSeek-v3, sequence粒度的
+    负载均衡loss): the expert-level balance loss of the ST-MoE section, computed within each
+    sequence instead of over the batch, averaged over the sequences. The page prints no formula;
+    the reading taken is L_seq = (1/B) sum_b L_B(tokens of sequence b), with f and P of each
+    sequence defined as for the batch. The batch is B = T / seq_len consecutive sequences.
+    -> (per-sequence losses [B], their mean)."""
+    u, s = _f64(u), _f64(s)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    T = u.shape[0]
+    assert seq_len > 0 and T % seq_len == 0
+    per = np.array([load_stats(cfg, u[b:b + seq_len], s[b:b + seq_len], idx[b:b + seq_len]).lb
+                    for b in range(0, T, seq_len)], dtype=np.float64)
+    return per, float(per.mean())
+
+
 def capacity_drop(cfg, idx, w) -> np.ndarray:
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     w = _f64(w)

@@ -364,6 +364,21 @@ def test_bias_update_sign_rule():
     np.testing.assert_array_equal(b, [-0.001, 0.001, 0.0, 0.0])
 
 
+def test_bias_update_fractional_mean_and_balance():
+    """A fractional mean leaves no expert at it; a perfectly balanced batch changes nothing;
+    every step is exactly +u, -u or 0 and moves each bias against its expert's load."""
+    b0 = np.array([0.5, -0.25, 0.125])
+    b = oracle.bias_update(np.array([3, 4, 4]), 0.25, b0)     # mean 11/3
+    np.testing.assert_array_equal(b - b0, [0.25, -0.25, -0.25])
+    np.testing.assert_array_equal(oracle.bias_update(np.full(8, 7), 0.5, np.arange(8.0)),
+                                  np.arange(8.0))
+    rng = np.random.default_rng(3)
+    c = rng.integers(0, 100, 64)
+    d = oracle.bias_update(c, 0.125, np.zeros(64))
+    assert set(np.unique(d)) <= {-0.125, 0.0, 0.125}
+    assert np.all((d > 0) == (c * 64 < c.sum())) and np.all((d < 0) == (c * 64 > c.sum()))
+
+
 def test_swiglu_bf16_weights_equal_widened_f64():
     """The bf16-weight entry widens exactly: same result as the fp64 entry on the same values."""
     g = torch.Generator().manual_seed(19)
@@ -373,3 +388,51 @@ def test_swiglu_bf16_weights_equal_widened_f64():
     a = oracle.swiglu_rows(x, w13, w2)
     b = oracle.swiglu_rows(x, w13.to(torch.float64).numpy(), w2.to(torch.float64).numpy())
     np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------------ sequence-wise balance loss
+def _uniform_stats_inputs(N, K, T, shift0=0):
+    """Logits whose routing gives every expert exactly T K / N assignments and P_e = 1/N:
+    token t's logit vector is a fixed base vector cyclically shifted by (shift0 + t K) mod N."""
+    base = np.linspace(3.0, -3.0, N)
+    u = np.stack([np.roll(base, (shift0 + t * K) % N) for t in range(T)])
+    return u
+
+
+def test_seq_balance_one_sequence_is_batch_loss():
+    cfg = CONFIGS["tiny"]
+    rng = np.random.default_rng(5)
+    u = rng.normal(0, 1, (cfg.T, cfg.n_routed))
+    s = oracle.scores(u, cfg.score_fn)
+    idx, _, _ = oracle.route(cfg, s, np.zeros(cfg.n_routed))
+    per, mean = oracle.seq_balance_loss(cfg, u, s, idx, cfg.T)
+    assert per.shape == (1,)
+    assert mean == oracle.load_stats(cfg, u, s, idx).lb
+
+
+def test_seq_balance_uniform_sequences_give_one():
+    """Routing uniform inside every sequence: each sequence's loss is 1, so is the mean."""
+    cfg = CONFIGS["v1"].replace(T=256, n_routed=16, top_k=4)
+    N, K, L = 16, 4, 64
+    u = _uniform_stats_inputs(N, K, cfg.T)
+    s = oracle.scores(u, "softmax")
+    idx, _, _ = oracle.route(cfg, s, None)
+    per, mean = oracle.seq_balance_loss(cfg, u, s, idx, L)
+    np.testing.assert_allclose(per, 1.0, rtol=1e-12)
+    assert abs(mean - 1.0) < 1e-12
+
+
+def test_seq_balance_sees_imbalance_the_batch_loss_hides():
+    """Each sequence sends all its tokens to its own K experts with equal scores there: every
+    sequence is collapsed (loss N / K) while the batch as a whole is perfectly balanced
+    (loss 1). The sequence-wise loss must report the collapse."""
+    N, K, L = 16, 4, 32
+    cfg = CONFIGS["v1"].replace(T=L * (N // K), n_routed=N, top_k=K)
+    u = np.full((cfg.T, N), -40.0)
+    for b in range(N // K):
+        u[b * L:(b + 1) * L, b * K:(b + 1) * K] = 0.0
+    s = oracle.scores(u, "softmax")
+    idx, _, _ = oracle.route(cfg, s, None)
+    per, mean = oracle.seq_balance_loss(cfg, u, s, idx, L)
+    np.testing.assert_allclose(per, N / K, rtol=1e-12)
+    assert abs(oracle.load_stats(cfg, u, s, idx).lb - 1.0) < 1e-12
