@@ -93,11 +93,9 @@ struct SmemCtl {
   int nprob;
   int total_tiles;
   int tile_start[MAXP + 1];
-  int row0[MAXP];
-  int rows[MAXP];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 template <int MODE>
@@ -142,7 +140,11 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   Tile t;
   t.prob = lo;
   t.shared = (MODE != MODE_GATE) && lo >= p.n_routed;
-  const int rows = c.rows[lo];
+  int row0 = 0, rows = p.T;
+  if (MODE != MODE_GATE && !t.shared) {
+    row0 = __ldg(p.offsets + lo);
+    rows = __ldg(p.offsets + lo + 1) - row0;
+  }
   const int ntt = (rows + TOK - 1) / TOK;
   const int local = tile - c.tile_start[lo];
   const int ft = local / ntt;
@@ -150,7 +152,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   t.f0 = ft * 2 * feat_per_cta<MODE>();
   // a segment's rows split into ntt token tiles of equal size (a multiple of 16)
   const int per = (((rows + ntt - 1) / ntt) + 15) & ~15;
-  t.r0 = c.row0[lo] + tt * per;
+  t.r0 = row0 + tt * per;
   t.nrows = min(per, rows - tt * per);
   t.ncols = (t.nrows + 15) & ~15;
   const int half = t.ncols / 2;
@@ -243,10 +245,13 @@ __device__ __forceinline__ void store_bf16_chunk(const float (&v)[NT], __nv_bflo
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms want 1 KB alignment
-  uint8_t* sgen = smem_raw + (sbase - raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);  // 128-byte swizzle atoms want 1 KB alignment
+  uint8_t* sgen = smem_raw;
+  if (sbase & 1023u) {  // not expected: report it instead of computing with a wrong layout
+    if (threadIdx.x == 0) set_error(p.err, ERR_DEVICE_CHECK);
+    return;
+  }
   SmemCtl& c = *reinterpret_cast<SmemCtl*>(sgen + (size_t)STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();   // 0: issues the MMA; 1: its peer
@@ -263,19 +268,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(&c.tmem_base), TMEM_COLS);
 
-  // ---- problem table and tile prefix (tile counts depend on device-resident offsets)
+  // ---- tile prefix over problems (tile counts depend on device-resident offsets)
   const int nprob = (MODE == MODE_GATE) ? 1 : p.n_routed + p.has_shared;
-  for (int q = threadIdx.x; q < nprob; q += THREADS) {
-    if (MODE != MODE_GATE && q < p.n_routed) {
-      const int r0 = p.offsets[q];
-      c.row0[q] = r0;
-      c.rows[q] = p.offsets[q + 1] - r0;
-    } else {
-      c.row0[q] = 0;
-      c.rows[q] = p.T;
-    }
-  }
-  __syncthreads();
   if (warp == 0) {
     int run = 0;
     for (int b = 0; b < nprob; b += 32) {
@@ -283,7 +277,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       int cnt = 0;
       if (q < nprob) {
         const bool sh = (MODE != MODE_GATE) && q >= p.n_routed;
-        const int rows = c.rows[q] > 0 ? c.rows[q] : 0;
+        int rows = p.T;
+        if (MODE != MODE_GATE && !sh) rows = max(p.offsets[q + 1] - p.offsets[q], 0);
         cnt = ((rows + TOK - 1) / TOK) * n_feat_tiles<MODE>(p, sh);
       }
       int incl = cnt;
