@@ -35,6 +35,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stages", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="launch every step eagerly instead of replaying a captured CUDA graph")
     return p.parse_args()
 
 
@@ -193,33 +195,48 @@ def run_ours(args, world, rank, local):
     # gate, route, permute (hist, scan, scatter, dispatch), up, down, combine (+ drop, + stats)
     launches_per_step = 9 + (1 if cfg.capacity_drop else 0) + (3 if want_stats else 0)
 
-    def step():
+    def step(s):
         moe.moe_layer_forward(cfg, T, x, w, out, counts if want_stats else None,
-                              lbz if want_stats else None, ws, stream)
+                              lbz if want_stats else None, ws, s)
 
     for _ in range(args.warmup):
-        step()
+        step(stream)
     st = moe.moe_get_error(stream)
     if st != 0:
         raise RuntimeError(f"device error {st} during warm-up")
 
     # ---- device-timed region (inputs resident in HBM; expert weights far above L2). The
     # library records a CUDA event on the launching stream at every stage boundary, so the
-    # per-kernel times below come from these same timed steps.
+    # per-kernel times below come from these same timed steps. By default the K steps are
+    # captured once into a CUDA graph (launch overheads matter for small decode batches) and
+    # the graph is replayed once untimed, then once timed.
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
     if not args.no_stages:
         moe.moe_stage_timing_start(args.steps)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            cs = torch.cuda.current_stream(dev)
+            for _ in range(args.steps):
+                step(cs)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         ev0.record(stream)
-        for _ in range(args.steps):
-            step()
+        if graph is not None:
+            graph.replay()
+        else:
+            for _ in range(args.steps):
+                step(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
     ms = ev0.elapsed_time(ev1)
     stages, ncalls = moe.moe_stage_timing_stop() if not args.no_stages else ({}, 0)
+    del graph
     st = moe.moe_get_error(stream)
     if st != 0:
         raise RuntimeError(f"device error {st} in the timed region")
@@ -252,6 +269,7 @@ def run_ours(args, world, rank, local):
                          "(L2 126 MB), no flush" % (work["weight_bytes"] / 1e9),
                    "kept_rows": kept_rows, "touched_experts": work["touched"]},
         "gpu_launches": launches_per_step * args.steps,
+        "launch": "CUDA graph of the timed steps" if not args.no_graph else "eager",
     }
     t_flop = work["flops"] / (pk["bf16"] * 1e12)
     t_byte = work["bytes"] / (pk["hbm_gbs"] * 1e9)
@@ -300,16 +318,33 @@ def run_ours(args, world, rank, local):
         xh = x.cpu().pin_memory()
         oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         xd = torch.empty_like(x)
-        for i in range(args.warmup + args.steps):
-            if i == args.warmup:
-                barrier(world)
-                torch.cuda.synchronize(dev)
-                ev0.record(stream)
+
+        def e2e_step(s):
             xd.copy_(xh, non_blocking=True)
-            moe.moe_layer_forward(cfg, T, xd, w, out, None, None, ws, stream)
+            moe.moe_layer_forward(cfg, T, xd, w, out, None, None, ws, s)
             oh.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step(stream)
+        graph = None
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+                cs = torch.cuda.current_stream(dev)
+                for _ in range(args.steps):
+                    e2e_step(cs)
+            graph.replay()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for _ in range(args.steps):
+                e2e_step(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+        del graph
         e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
         result["e2e"] = {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                          "h2d_bytes_per_step": xh.numel() * xh.element_size(),

@@ -245,6 +245,8 @@ moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float r
  *   0 gate GEMM, 1 routing, 2 load statistics (zero when not requested), 3 permutation
  *   (drop thresholds, histogram, scan, scatter), 4 row dispatch (x -> x_perm), 5 expert up
  *   GEMM (routed + shared, SwiGLU), 6 expert down GEMM, 7 combine.
+ * Calls captured into a CUDA graph record their events as graph nodes, which record each time
+ * the graph runs; stop then reads the last run's times.
  * moe_stage_timing_start creates the events (host resources only, no device memory).
  * moe_stage_timing_stop waits for the recorded events, writes the summed milliseconds of the
  * first n_stages stages over the recorded calls to stage_ms (may be NULL), the number of

@@ -102,7 +102,7 @@ size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 // Workspace carve for one config and token count. Every region is 256-byte aligned.
 struct Layout {
   size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_lse,
-      counts, seq_s, seq_c, seq_lb, xy_perm, h, h_sh, y_sh, total;
+      counts, seq_s, seq_c, seq_lb, gate_part, xy_perm, h, h_sh, y_sh, total;
 };
 
 Layout layout(const moe_config* c, int32_t T) {
@@ -133,6 +133,7 @@ Layout layout(const moe_config* c, int32_t T) {
   L.seq_s = take(seq_rows * N * 4);
   L.seq_c = take(seq_rows * N * 4);
   L.seq_lb = take(Tt * 8);
+  L.gate_part = take((size_t)GATE_PART_ROWS * N * 4);
   L.xy_perm = take(A * H * eb);   // x_perm, then reused for y_perm
   L.h = take(A * I * eb);
   L.h_sh = take(Tt * (S > 0 ? S : 1) * I * eb);
@@ -196,19 +197,30 @@ struct StageTiming {
 StageTiming g_timing;
 
 // Boundary b (the start of stage b; b == N_STAGES is the end of the call) of the current call.
+// Under stream capture the record becomes an event-record node of the graph (it then records
+// each time the graph runs).
 void stage_mark(int b, cudaStream_t st) {
   if (!g_timing.on || g_timing.cur < 0) return;
-  cudaEventRecord(g_timing.ev[(size_t)g_timing.cur * (N_STAGES + 1) + b], st);
+  cudaEvent_t ev = g_timing.ev[(size_t)g_timing.cur * (N_STAGES + 1) + b];
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, st);
 }
 
 // ---------------------------------------------------------------- step implementations
 moe_status do_gate(const moe_config* c, int32_t T, const void* x, const moe_weights* w, float* u,
-                   cudaStream_t st) {
+                   void* ws, cudaStream_t st) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_GATE;
   g.T = T; g.H = c->hidden; g.I = c->inter; g.S = c->n_shared; g.N = c->n_routed;
   g.a0 = x; g.b0 = w->w_gate; g.out0 = u; g.gate_bias = w->gate_logit_bias;
+  if (ws != nullptr) {  // split-K scratch for few-token batches
+    g.gate_part = at<float>(ws, layout(c, T).gate_part);
+    g.gate_part_floats = (size_t)GATE_PART_ROWS * c->n_routed;
+  }
   g.err = error_word();
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "gate GEMM");
@@ -335,7 +347,7 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
   void* y_sh = cfg->n_shared > 0 ? at<char>(ws, L.y_sh) : nullptr;
 
   stage_mark(STAGE_GATE, st);
-  TRY(do_gate(cfg, T, x, w, u, st));
+  TRY(do_gate(cfg, T, x, w, u, ws, st));
   stage_mark(STAGE_ROUTE, st);
   TRY(do_route(cfg, T, u, w, idx, wt, st));
   stage_mark(STAGE_STATS, st);
@@ -392,7 +404,9 @@ moe_status moe_route(const moe_config* cfg, int32_t T, const void* x, const moe_
       TRY(check_ws(cfg, T, ws, ws_bytes));
       dst = at<float>(ws, layout(cfg, T).u);
     }
-    TRY(do_gate(cfg, T, x, w, dst, S_(stream)));
+    // the workspace, when one is given, also holds the split-K scratch of small batches
+    const bool ws_ok = ws != nullptr && ws_bytes >= layout(cfg, T).total && aligned16(ws);
+    TRY(do_gate(cfg, T, x, w, dst, ws_ok ? ws : nullptr, S_(stream)));
     u = dst;
   } else {
     CHECK_PTR(logits_in);

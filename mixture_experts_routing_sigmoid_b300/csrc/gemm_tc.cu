@@ -79,6 +79,8 @@ struct TcParams {
   void* out0;
   void* out1;
   const float* gate_bias;
+  float* gate_part;          // GATE split-K: partial sums [splits][T][N]
+  int splits, kb_per_split;  // GATE: K range split over `splits` tiles (1 = no split)
   int* err;
 };
 
@@ -126,7 +128,8 @@ struct Tile {
   int ncols;     // MMA N: nrows rounded up to 16; each CTA holds ncols / 2 token rows
   int nbox;      // token boxes loaded per CTA and stage
   bool big_box;  // boxes of 64 rows (else one box of 32)
-  int kb;        // k blocks
+  int kb0, kb;   // first k block and k blocks (GATE split-K: this split's range)
+  int split;     // GATE split-K: which split
   bool shared;
 };
 
@@ -146,7 +149,13 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
     rows = __ldg(p.offsets + lo + 1) - row0;
   }
   const int ntt = (rows + TOK - 1) / TOK;
-  const int local = tile - c.tile_start[lo];
+  int local = tile - c.tile_start[lo];
+  t.split = 0;
+  if (MODE == MODE_GATE && p.splits > 1) {  // split outermost
+    const int per_split = ntt * n_feat_tiles<MODE>(p, false);
+    t.split = local / per_split;
+    local -= t.split * per_split;
+  }
   const int ft = local / ntt;
   const int tt = local - ft * ntt;
   t.f0 = ft * 2 * feat_per_cta<MODE>();
@@ -158,7 +167,12 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   const int half = t.ncols / 2;
   t.big_box = half > XBOX_S;
   t.nbox = t.big_box ? (half + XBOX_L - 1) / XBOX_L : 1;
+  t.kb0 = 0;
   t.kb = k_blocks_of<MODE>(p, t.shared);
+  if (MODE == MODE_GATE && p.splits > 1) {
+    t.kb0 = t.split * p.kb_per_split;
+    t.kb = min(p.kb_per_split, t.kb - t.kb0);
+  }
   return t;
 }
 
@@ -280,6 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         int rows = p.T;
         if (MODE != MODE_GATE && !sh) rows = max(p.offsets[q + 1] - p.offsets[q], 0);
         cnt = ((rows + TOK - 1) / TOK) * n_feat_tiles<MODE>(p, sh);
+        if (MODE == MODE_GATE) cnt *= p.splits;
       }
       int incl = cnt;
 #pragma unroll
@@ -326,7 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         const uint32_t fb = mapa_shared(bar(c.full[stage]), 0);  // the first CTA's barrier
         const uint32_t sa = sbase + stage * STAGE_BYTES;
         const uint32_t sb = sa + A_BYTES;
-        const Boxes b = boxes_of<MODE>(p, t, kb, rank);
+        const Boxes b = boxes_of<MODE>(p, t, t.kb0 + kb, rank);
         if (lane == 0) {
           if (rank == 0) mbar_expect_tx(bar(c.full[stage]), 2 * (A_BYTES + t.nbox * b.box_bytes));
           if (MODE == MODE_UP) tma_load_5d_pair(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1);
@@ -449,8 +464,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             store_bf16_chunk<32>(yv, static_cast<__nv_bfloat16*>(t.shared ? p.out1 : p.out0), p.H,
                                  row0, nvalid, f, fvalid, lane);
           } else {
-            float* out = static_cast<float*>(p.out0) + row0 * p.N + f;
-            const float bias = (fvalid && p.gate_bias) ? p.gate_bias[f] : 0.0f;
+            // split-K: partial sums of this split (the reduction adds the bias)
+            float* out = (p.splits > 1 ? p.gate_part + (size_t)t.split * p.T * p.N
+                                       : static_cast<float*>(p.out0)) + row0 * p.N + f;
+            const float bias = (p.splits == 1 && fvalid && p.gate_bias) ? p.gate_bias[f] : 0.0f;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (fvalid && i < nvalid) out[(size_t)i * p.N] = __uint_as_float(v[i]) + bias;
@@ -468,6 +485,18 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   cluster_sync();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+// u[t, e] = gate_bias[e] + sum over splits s (in order) of part[s, t, e].
+__global__ void __launch_bounds__(256) gate_reduce_kernel(const float* part, int splits, int T,
+                                                          int N, const float* bias, float* u) {
+  const size_t n = (size_t)T * N;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float acc = bias ? bias[i % N] : 0.0f;
+    for (int s = 0; s < splits; ++s) acc += part[(size_t)s * n + i];
+    u[i] = acc;
+  }
 }
 
 // One CTA waits on an mbarrier that nothing ever arrives on; the bounded wait must give up,
@@ -580,13 +609,36 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   prm.T = a.T; prm.H = a.H; prm.I = a.I; prm.S = a.S; prm.N = a.N;
   prm.out0 = a.out0; prm.out1 = a.out1;
   prm.gate_bias = a.gate_bias;
+  prm.splits = 1;
   prm.err = a.err;
   const uint64_t H = a.H, I = a.I, S = a.S, N = a.N, T = a.T, R = a.rows_cap;
   bool ok = true;
   if (a.mode == MODE_GATE) {
     ok = make_map(&prm.tmW0, a.b0, H, N, BM) && make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, T);
     if (!ok) return cudaErrorInvalidValue;
-    return launch_mode<MODE_GATE>(prm, num_sms, st);
+    // Few token tiles (decode): split the K range so that about every CTA pair has a tile;
+    // the partial sums go to the caller's scratch and are reduced in a fixed order.
+    const int tiles = (int)((T + TOK - 1) / TOK) * (int)((N + 2 * BM - 1) / (2 * BM));
+    const int kb_total = (int)(H / BK);
+    const int pairs = num_sms / 2;
+    if (a.gate_part != nullptr && 2 * tiles <= pairs) {
+      int want = pairs / tiles;
+      const size_t fit = a.gate_part_floats / ((size_t)T * N);
+      if ((size_t)want > fit) want = (int)fit;
+      if (want > kb_total) want = kb_total;
+      if (want > 1) {
+        prm.kb_per_split = (kb_total + want - 1) / want;
+        prm.splits = (kb_total + prm.kb_per_split - 1) / prm.kb_per_split;
+        prm.gate_part = a.gate_part;
+      }
+    }
+    cudaError_t e = launch_mode<MODE_GATE>(prm, num_sms, st);
+    if (e != cudaSuccess || prm.splits == 1) return e;
+    int blocks = (int)(((size_t)T * N + 255) / 256);
+    if (blocks > num_sms * 8) blocks = num_sms * 8;
+    gate_reduce_kernel<<<blocks, 256, 0, st>>>(a.gate_part, prm.splits, (int)T, (int)N, a.gate_bias,
+                                               static_cast<float*>(a.out0));
+    return cudaGetLastError();
   }
   if (a.mode == MODE_UP) {
     if (a.n_routed > 0) ok = ok && make_up_weight_map(&prm.tmW0, a.b0, H, I, N) &&

@@ -111,8 +111,12 @@ struct GemmArgs {
   void* out0;               // routed out: h [rows_cap,I] | y [rows_cap,H] | u [T,N] fp32
   void* out1;               // shared out: h_shared [T,S*I] | y_shared [T,H]
   const float* gate_bias;   // MODE_GATE: [N] or nullptr
+  float* gate_part;         // MODE_GATE split-K partial sums, or nullptr (no split)
+  size_t gate_part_floats;  // capacity of gate_part
   int* err;
 };
+// Rows (of N floats) of the gate GEMM's split-K scratch the workspace provides.
+constexpr int GATE_PART_ROWS = 16384;
 // bf16 on tcgen05 / TMEM / TMA (gemm_tc.cu)
 cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st);
 // fp32 on CUDA cores (gemm_simt.cu)
