@@ -192,8 +192,6 @@ def run_ours(args, world, rank, local):
     counts = torch.empty(N, dtype=torch.int32, device=dev)
     lbz = torch.empty(3, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    # gate, route, permute (hist, scan, scatter, dispatch), up, down, combine (+ drop, + stats)
-    launches_per_step = 9 + (1 if cfg.capacity_drop else 0) + (3 if want_stats else 0)
 
     def step(s):
         moe.moe_layer_forward(cfg, T, x, w, out, counts if want_stats else None,
@@ -214,12 +212,14 @@ def run_ours(args, world, rank, local):
     if not args.no_stages:
         moe.moe_stage_timing_start(args.steps)
     graph = None
+    launches0 = moe.moe_kernel_launches()
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, capture_error_mode="relaxed"):
             cs = torch.cuda.current_stream(dev)
             for _ in range(args.steps):
                 step(cs)
+        launches = moe.moe_kernel_launches() - launches0  # what each replay runs
         graph.replay()
         torch.cuda.synchronize(dev)
     barrier(world)
@@ -233,6 +233,8 @@ def run_ours(args, world, rank, local):
                 step(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+    if graph is None:
+        launches = moe.moe_kernel_launches() - launches0
     barrier(world)
     ms = ev0.elapsed_time(ev1)
     stages, ncalls = moe.moe_stage_timing_stop() if not args.no_stages else ({}, 0)
@@ -268,7 +270,7 @@ def run_ours(args, world, rank, local):
                    "l2": "inputs larger than L2: expert weights touched per step %.2f GB "
                          "(L2 126 MB), no flush" % (work["weight_bytes"] / 1e9),
                    "kept_rows": kept_rows, "touched_experts": work["touched"]},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches,
         "launch": "CUDA graph of the timed steps" if not args.no_graph else "eager",
     }
     t_flop = work["flops"] / (pk["bf16"] * 1e12)

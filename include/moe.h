@@ -266,6 +266,11 @@ moe_status moe_get_error(moe_stream_t stream);
  * with moe_get_error(). No fault, no trap, the context stays usable. */
 moe_status moe_selftest_wait_timeout(int32_t timeout_us, moe_stream_t stream);
 
+/* Number of kernels this library has launched in this process so far (all devices, all
+ * streams; a launch made while a stream is captured into a CUDA graph counts once, at capture).
+ * Host-only counter, for measurement. */
+unsigned long long moe_kernel_launches(void);
+
 /* Static text for a status code. */
 const char* moe_status_string(moe_status s);
 

@@ -16,7 +16,7 @@ __all__ = ["MoeError", "MoeConfig", "MoeWeights", "lib", "make_config", "make_we
            "moe_expert_ffn", "moe_expert_up", "moe_expert_down", "moe_combine",
            "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
            "moe_status_string", "moe_permute_static_scratch", "moe_stage_timing_start",
-           "moe_stage_timing_stop", "moe_bias_update", "moe_seq_balance_loss", "STAGE_NAMES", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
+           "moe_stage_timing_stop", "moe_bias_update", "moe_seq_balance_loss", "moe_kernel_launches", "STAGE_NAMES", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
            "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT",
            "MOE_ERR_DEVICE_CHECK"]
 
@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_load_stats", "moe_pe
                     "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
                     "moe_status_string", "moe_last_error_detail", "moe_permute_static_scratch",
                     "moe_stage_timing_start", "moe_stage_timing_stop", "moe_bias_update",
-                    "moe_seq_balance_loss")
+                    "moe_seq_balance_loss", "moe_kernel_launches")
 
 # Stages of moe_layer_forward as moe_stage_timing_stop reports them (MOE_N_STAGES).
 STAGE_NAMES = ("gate", "route", "stats", "permute", "dispatch", "up", "down", "combine")
@@ -86,6 +86,7 @@ def _load():
         "moe_stage_timing_start": (I32, [I32]),
         "moe_bias_update": (I32, [CFG, P, ctypes.c_float, P, P]),
         "moe_seq_balance_loss": (I32, [CFG, I32, I32, P, P, P, P, P, SZ, P]),
+        "moe_kernel_launches": (ctypes.c_ulonglong, []),
         "moe_stage_timing_stop": (I32, [P, I32, P]),
     }
     for name, (res, args) in sig.items():
@@ -263,3 +264,8 @@ def moe_seq_balance_loss(cfg, T, seq_len, logits, topk_idx, per_seq, loss, ws, s
     _check(lib.moe_seq_balance_loss(ctypes.byref(_cfg(cfg)), int(T), int(seq_len), _ptr(logits),
                                     _ptr(topk_idx), _ptr(per_seq), _ptr(loss), p, n,
                                     _stream(stream)), "moe_seq_balance_loss")
+
+
+def moe_kernel_launches() -> int:
+    """Kernels launched by the library so far (a graph-captured launch counts once)."""
+    return int(lib.moe_kernel_launches())

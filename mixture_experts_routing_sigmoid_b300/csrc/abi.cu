@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <new>
 
 #include "../../include/moe.h"
@@ -367,6 +368,10 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
 
 // Accessors for other entry-point files of this library (same checks, same error reporting).
 namespace moe {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 moe_status abi_check_config(const moe_config* c, int32_t T) {
   g_detail[0] = 0;
   return check_cfg(c, T);
@@ -677,5 +682,7 @@ const char* moe_status_string(moe_status s) {
 }
 
 const char* moe_last_error_detail(void) { return g_detail; }
+
+unsigned long long moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -153,6 +153,7 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t st) {
   // routed rows of one expert never exceed T (a token picks an expert at most once)
   dim3 grid((ncols_max + TN - 1) / TN, (a.T + TM - 1) / TM, probs);
   simt_gemm_kernel<<<grid, 256, 0, st>>>(a);
+  note_launches(1);
   return cudaGetLastError();
 }
 

@@ -594,6 +594,7 @@ cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
     if (dev >= 0 && dev < 64) grid_for_device[dev] = grid;
   }
   cfg.gridDim = dim3(grid, 1, 1);
+  note_launches(1);
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, prm);
 }
 
@@ -638,6 +639,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
     if (blocks > num_sms * 8) blocks = num_sms * 8;
     gate_reduce_kernel<<<blocks, 256, 0, st>>>(a.gate_part, prm.splits, (int)T, (int)N, a.gate_bias,
                                                static_cast<float*>(a.out0));
+    note_launches(1);
     return cudaGetLastError();
   }
   if (a.mode == MODE_UP) {
@@ -658,6 +660,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long timeout_ns, cudaStream_t st) {
   wait_selftest_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
+  note_launches(1);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,9 @@
 
 namespace moe {
 
+// Count of kernels this library has launched (abi.cu); every launcher adds its launches.
+void note_launches(int n);
+
 // ---------------------------------------------------------------- routing (route.cu)
 struct RouteArgs {
   int T, N, K, G, Gk, topn, score_fn, norm_topk, precise_w;

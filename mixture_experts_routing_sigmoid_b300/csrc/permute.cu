@@ -8,7 +8,7 @@
 //   1. per 256-token block, a bitmask per expert of the block's tokens that chose it;
 //   2. one CTA scans counts over blocks and experts -> segment offsets, per-block bases;
 //   3. a token's row = base + number of earlier tokens of its block in the expert's mask;
-//   4. one warp per token copies x[t] once to each of its rows.
+//   4. one thread per 16-byte chunk of x[t] copies it once to each of the token's rows.
 // Drop ("DeepSeek MoE：从v1到v3的演进", DeepSeek-v2 device-level token drop): device d of the G
 // virtual devices keeps its C = ceil(T K / G) best assignments by (fp32 weight desc, token asc,
 // slot asc). One CTA per device radix-selects the C-th largest 64-bit key
@@ -154,24 +154,87 @@ __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
   }
 }
 
-// One warp per token: read x[t] once in 16-byte chunks, write it to every kept row.
+// Batches of at most one block (T <= 256): histogram, scan and scatter in one CTA, the same
+// arithmetic as the three kernels above with the per-block state kept in shared memory.
+__global__ void __launch_bounds__(PB) perm_single_block_kernel(PermuteArgs p) {
+  extern __shared__ uint32_t sm[];  // [N][8] masks, then [N + 1] exclusive offsets
+  int* excl = reinterpret_cast<int*>(sm + p.N * 8);
+  for (int i = threadIdx.x; i < p.N * 8; i += PB) sm[i] = 0;
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t < p.T) {
+    for (int k = 0; k < p.K; ++k) {
+      const long long a = (long long)t * p.K + k;
+      const int e = p.idx[a];
+      if (e < 0 || e >= p.N) { set_error(p.err, ERR_DEVICE_CHECK); continue; }
+      if (is_kept(p, a, e)) atomicOr(&sm[e * 8 + (t >> 5)], 1u << (t & 31));
+    }
+  }
+  __syncthreads();
+  {
+    // exclusive scan of the per-expert counts (N <= 256 = PB): warp scans, then warp totals
+    __shared__ int wsum[PB / 32];
+    const int e = threadIdx.x, lane = e & 31, wi = e >> 5;
+    int cnt = 0;
+    if (e < p.N) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) cnt += __popc(sm[e * 8 + w]);
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[wi] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < wi; ++i) before += wsum[i];
+    if (e < p.N) {
+      excl[e] = before + incl - cnt;
+      p.offsets[e] = before + incl - cnt;
+    }
+    if (e == p.N - 1) {
+      excl[p.N] = before + incl;
+      p.offsets[p.N] = before + incl;
+    }
+  }
+  __syncthreads();
+  if (t < p.T) {
+    const int wi = t >> 5;
+    const uint32_t below = (1u << (t & 31)) - 1u;
+    for (int k = 0; k < p.K; ++k) {
+      const long long a = (long long)t * p.K + k;
+      const int e = p.idx[a];
+      if (e < 0 || e >= p.N || !is_kept(p, a, e)) { p.slot_row[a] = -1; continue; }
+      const uint32_t* m = sm + e * 8;
+      int rank = __popc(m[wi] & below);
+      for (int i = 0; i < wi; ++i) rank += __popc(m[i]);
+      const int row = excl[e] + rank;
+      p.slot_row[a] = row;
+      p.row_token[row] = t;
+    }
+  }
+}
+
+// One thread per 16-byte chunk of a token's row: read it once, write it to each kept row of
+// the token. Consecutive threads take consecutive chunks of a row, so every warp reads and
+// writes contiguous runs; a batch of a few tokens still spreads over the whole GPU.
 __global__ void __launch_bounds__(256) dispatch_rows_kernel(PermuteArgs p) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
   const size_t row_bytes = (size_t)p.H * p.elem_bytes;
   const int chunks = (int)(row_bytes / 16);
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < p.T; t += warps) {
-    const int my = lane < p.K ? p.slot_row[(size_t)t * p.K + lane] : -1;
-    int rows[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) rows[k] = __shfl_sync(FULL_MASK, my, k);
-    const char* src = static_cast<const char*>(p.x) + (size_t)t * row_bytes;
-    char* dst = static_cast<char*>(p.x_perm);
-    for (int c = lane; c < chunks; c += 32) {
-      const uint4 v = ld_nc_v4(src + (size_t)c * 16);
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (k < p.K && rows[k] >= 0) st_v4(dst + (size_t)rows[k] * row_bytes + (size_t)c * 16, v);
+  const size_t n = (size_t)p.T * chunks;
+  const char* src = static_cast<const char*>(p.x);
+  char* dst = static_cast<char*>(p.x_perm);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / chunks);
+    const int c = (int)(i - (size_t)t * chunks);
+    const uint4 v = ld_nc_v4(src + (size_t)t * row_bytes + (size_t)c * 16);
+    const int32_t* sr = p.slot_row + (size_t)t * p.K;
+    for (int k = 0; k < p.K; ++k) {
+      const int r = __ldg(sr + k);
+      if (r >= 0) st_v4(dst + (size_t)r * row_bytes + (size_t)c * 16, v);
     }
   }
 }
@@ -188,18 +251,27 @@ cudaError_t launch_permute(const PermuteArgs& p, int num_sms, cudaStream_t st) {
   const int nb = permute_blocks(p.T);
   if (p.capacity_drop) {
     drop_threshold_kernel<<<p.D, 1024, 0, st>>>(p);
+    note_launches(1);
+  }
+  if (nb == 1) {
+    perm_single_block_kernel<<<1, PB, (p.N * 8 + p.N + 1) * sizeof(uint32_t), st>>>(p);
+    note_launches(1);
+    return cudaGetLastError();
   }
   perm_hist_kernel<<<nb, PB, p.N * 8 * sizeof(uint32_t), st>>>(p);
   perm_scan_kernel<<<1, 256, 0, st>>>(p, nb);
   perm_scatter_kernel<<<nb, PB, 0, st>>>(p);
+  note_launches(3);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch(const PermuteArgs& p, int num_sms, cudaStream_t st) {
   if (p.T <= 0 || p.x == nullptr || p.x_perm == nullptr) return cudaSuccess;
-  int blocks = (p.T + 7) / 8;
-  if (blocks > num_sms * 8) blocks = num_sms * 8;
-  dispatch_rows_kernel<<<blocks, 256, 0, st>>>(p);
+  const size_t n = (size_t)p.T * ((size_t)p.H * p.elem_bytes / 16);
+  size_t blocks = (n + 255) / 256;
+  if (blocks > (size_t)num_sms * 16) blocks = (size_t)num_sms * 16;
+  dispatch_rows_kernel<<<(int)blocks, 256, 0, st>>>(p);
+  note_launches(1);
   return cudaGetLastError();
 }
 

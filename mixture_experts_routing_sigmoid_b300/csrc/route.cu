@@ -71,26 +71,50 @@ __device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int l
   out.gkth = INFINITY;
   if (G > 1) {
     KT my_gs = neg_inf<KT>();
-    for (int g = 0; g < G; ++g) {
-      KT a1 = neg_inf<KT>(), a2 = neg_inf<KT>();
+    if (gsz == 32 && G == J) {
+      // group g is register g of every lane: reduce all groups' top-2 side by side
+      KT a1[MAXJ], a2[MAXJ];
 #pragma unroll
       for (int j = 0; j < MAXJ; ++j) {
-        const int e = j * 32 + lane;
-        if (j < J && e < N && e / gsz == g) {
-          const KT v = key[j];
-          if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
-        }
+        a1[j] = j < J ? key[j] : neg_inf<KT>();
+        a2[j] = neg_inf<KT>();
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const KT b1 = __shfl_xor_sync(FULL_MASK, a1, o);
-        const KT b2 = __shfl_xor_sync(FULL_MASK, a2, o);
-        const KT n1 = max(a1, b1);
-        const KT n2 = max(min(a1, b1), max(a2, b2));
-        a1 = n1; a2 = n2;
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j) {
+          const KT b1 = __shfl_xor_sync(FULL_MASK, a1[j], o);
+          const KT b2 = __shfl_xor_sync(FULL_MASK, a2[j], o);
+          const KT n2 = max(min(a1[j], b1), max(a2[j], b2));
+          a1[j] = max(a1[j], b1);
+          a2[j] = n2;
+        }
       }
-      const KT gsv = (topn == 1) ? a1 : a1 + a2;
-      if (lane == g) my_gs = gsv;
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j)
+        if (lane == j) my_gs = (topn == 1) ? a1[j] : a1[j] + a2[j];
+    } else {
+      for (int g = 0; g < G; ++g) {
+        KT a1 = neg_inf<KT>(), a2 = neg_inf<KT>();
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j) {
+          const int e = j * 32 + lane;
+          if (j < J && e < N && e / gsz == g) {
+            const KT v = key[j];
+            if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const KT b1 = __shfl_xor_sync(FULL_MASK, a1, o);
+          const KT b2 = __shfl_xor_sync(FULL_MASK, a2, o);
+          const KT n1 = max(a1, b1);
+          const KT n2 = max(min(a1, b1), max(a2, b2));
+          a1 = n1; a2 = n2;
+        }
+        const KT gsv = (topn == 1) ? a1 : a1 + a2;
+        if (lane == g) my_gs = gsv;
+      }
     }
     gmask = 0;
     bool taken = false;
@@ -400,6 +424,7 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   const int cap = num_sms * 8;
   if (blocks > cap) blocks = cap;
   route_kernel<<<blocks, 256, 0, st>>>(a);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -420,6 +445,7 @@ cudaError_t launch_stats(const StatsArgs& a, cudaStream_t st) {
   stats_count_kernel<<<cb, 256, 0, st>>>(a.idx, n, a.N, a.counts, a.err);
   stats_partial_kernel<<<a.nblk, 256, 0, st>>>(a);
   stats_final_kernel<<<1, 256, 0, st>>>(a);
+  note_launches(3);
   return cudaGetLastError();
 }
 
