@@ -23,6 +23,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (route+permute+expert FFN+combine); % of roofline"
+# A timed region at least this long runs under the power cap: use the sustained bf16 peak.
+LONG_REGION_MS = 500.0
 
 
 def parse():
@@ -273,14 +275,21 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches,
         "launch": "CUDA graph of the timed steps" if not args.no_graph else "eager",
     }
-    t_flop = work["flops"] / (pk["bf16"] * 1e12)
+    # Tensor peak: the measured sustained bf16 rate when the timed region is long (the GPU
+    # then runs under its power cap, as the sustained measurement did), else the burst rate.
+    sustained = ms_max >= LONG_REGION_MS
+    bf16_peak = pk["bf16_sus"] if sustained else pk["bf16"]
+    bf16_kind = ("bf16 sustained" if sustained else "bf16 burst") + ", " + pk["source"]
+    t_flop = work["flops"] / (bf16_peak * 1e12)
     t_byte = work["bytes"] / (pk["hbm_gbs"] * 1e9)
     t_roof = max(t_flop, t_byte)
     result["layer_roofline"] = {
         "flops": work["flops"], "bytes": work["bytes"], "roofline_ms": t_roof * 1e3,
         "frac": t_roof * 1e3 / ms_step, "tflops": work["flops"] / (ms_step * 1e-3) / 1e12,
         "weight_gbs": work["weight_bytes"] / (ms_step * 1e-3) / 1e9,
-        "bound": "tensor" if t_flop >= t_byte else "hbm", "peaks": pk["source"] + " burst"}
+        "bound": "tensor" if t_flop >= t_byte else "hbm",
+        "peaks": f"{bf16_kind} ({bf16_peak} TFLOP/s), HBM copy ({pk['hbm_gbs']} GB/s)",
+        "frac_vs_burst_peak": max(work["flops"] / (pk["bf16"] * 1e12), t_byte) * 1e3 / ms_step}
     result["clocks"] = clk.summary()
 
     # ---- the dominant kernel (the SwiGLU up GEMM) against its own roofline
@@ -292,10 +301,10 @@ def run_ours(args, world, rank, local):
             up_tf = work["up_flops"] / (up * 1e-3) / 1e12
             result["roofline"] = {
                 "kernel": "tc_gemm_kernel<MODE_UP> (grouped SwiGLU up projection, tcgen05)",
-                "bound": "tensor", "achieved": up_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": up_tf / pk["bf16"], "traffic": traffic,
-                "peak_kind": "bf16 burst, " + pk["source"],
-                "frac_of_sustained": up_tf / pk["bf16_sus"], "avg_launch_ms": up,
+                "bound": "tensor", "achieved": up_tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": up_tf / bf16_peak, "traffic": traffic,
+                "peak_kind": bf16_kind,
+                "frac_of_burst": up_tf / pk["bf16"], "avg_launch_ms": up,
                 "algorithmic_flops_per_launch": work["up_flops"]}
         else:
             gbs = work["up_weight_bytes"] / (up * 1e-3) / 1e9
