@@ -94,7 +94,9 @@ struct SmemCtl {
   int abort_flag;
   int nprob;
   int total_tiles;
-  int tile_start[MAXP + 1];
+  int tile_start[MAXP + 1];   // by position in `order`
+  int order[MAXP];            // problems, most rows first (ties: lower index)
+  int rows[MAXP];
 };
 
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
@@ -141,6 +143,8 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
     if (c.tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
   }
   Tile t;
+  const int pos = lo;
+  lo = c.order[pos];
   t.prob = lo;
   t.shared = (MODE != MODE_GATE) && lo >= p.n_routed;
   int row0 = 0, rows = p.T;
@@ -149,7 +153,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
     rows = __ldg(p.offsets + lo + 1) - row0;
   }
   const int ntt = (rows + TOK - 1) / TOK;
-  int local = tile - c.tile_start[lo];
+  int local = tile - c.tile_start[pos];
   t.split = 0;
   if (MODE == MODE_GATE && p.splits > 1) {  // split outermost
     const int per_split = ntt * n_feat_tiles<MODE>(p, false);
@@ -282,18 +286,34 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(&c.tmem_base), TMEM_COLS);
 
-  // ---- tile prefix over problems (tile counts depend on device-resident offsets)
+  // ---- problems in order of decreasing rows, so that the longest run first and the pairs
+  // finish together; then the tile prefix over that order (counts depend on device offsets)
   const int nprob = (MODE == MODE_GATE) ? 1 : p.n_routed + p.has_shared;
+  for (int q = threadIdx.x; q < nprob; q += THREADS) {
+    int rows = p.T;
+    if (MODE != MODE_GATE && q < p.n_routed) rows = max(p.offsets[q + 1] - p.offsets[q], 0);
+    c.rows[q] = rows;
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < nprob; q += THREADS) {
+    const int rq = c.rows[q];
+    int rank = 0;
+    for (int o = 0; o < nprob; ++o) {
+      const int ro = c.rows[o];
+      rank += (ro > rq || (ro == rq && o < q)) ? 1 : 0;
+    }
+    c.order[rank] = q;
+  }
+  __syncthreads();
   if (warp == 0) {
     int run = 0;
     for (int b = 0; b < nprob; b += 32) {
-      const int q = b + lane;
+      const int i = b + lane;       // position in the order
       int cnt = 0;
-      if (q < nprob) {
+      if (i < nprob) {
+        const int q = c.order[i];
         const bool sh = (MODE != MODE_GATE) && q >= p.n_routed;
-        int rows = p.T;
-        if (MODE != MODE_GATE && !sh) rows = max(p.offsets[q + 1] - p.offsets[q], 0);
-        cnt = ((rows + TOK - 1) / TOK) * n_feat_tiles<MODE>(p, sh);
+        cnt = ((c.rows[q] + TOK - 1) / TOK) * n_feat_tiles<MODE>(p, sh);
         if (MODE == MODE_GATE) cnt *= p.splits;
       }
       int incl = cnt;
@@ -302,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         const int v = __shfl_up_sync(FULL_MASK, incl, o);
         if (lane >= o) incl += v;
       }
-      if (q < nprob) c.tile_start[q] = run + incl - cnt;
+      if (i < nprob) c.tile_start[i] = run + incl - cnt;
       run += __shfl_sync(FULL_MASK, incl, 31);
     }
     if (lane == 0) { c.tile_start[nprob] = run; c.total_tiles = run; c.nprob = nprob; }

@@ -228,8 +228,17 @@ __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
              (sel.emargin > 0.0 && sel.emargin < tiny) ||
              (a.G > a.Gk && sel.gmargin > 0.0 && sel.gmargin < 1e-9 * fmax(1.0, fabs(sel.gkth)));
     } else {
+      // A group score is the fp32 sum of its top-n keys: it is off by at most n key errors
+      // (the n-th largest of perturbed values moves by at most the largest perturbation) plus
+      // the rounding of the sum.
+      float kmax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j)
+        if (j < J && j * 32 + lane < a.N) kmax = fmaxf(kmax, fabsf(key[j]));
+      kmax = warp_max(kmax);
+      const double gtol = a.topn * (double)key_tol(kmax) + 6e-8 * fabs(sel.gkth);
       redo = !sel.ok || sel.emargin <= 2.0 * key_tol(sel.kth) ||
-             (a.G > a.Gk && sel.gmargin <= 2.0 * (a.topn + 1) * key_tol(sel.gkth));
+             (a.G > a.Gk && sel.gmargin <= 2.0 * gtol);
     }
     redo = __any_sync(FULL_MASK, redo);
 
