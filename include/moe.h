@@ -210,6 +210,22 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Device-level and communication balance losses ([P3] DeepSeek-v1 "设备级负载loss", DeepSeek-v2
+ * "通信负载均衡loss"; the page describes them without formulas, so the expert-level loss of
+ * moe_load_stats is taken with the n_groups devices as its units, expert e on device e/(N/G)):
+ *   f'_d = sum_{e on d} counts[e] / (T K);   P'_d = sum_{e on d} P[e];
+ *   L_dev = G sum_d f'_d P'_d;
+ *   R_d = tokens with at least one chosen expert on d (tokens d receives);
+ *   L_comm = G sum_d (R_d / sum R) P'_d.
+ * Both are 1 when routing is uniform; with one expert per device L_dev is the expert-level L_B.
+ *   logits [T, N] fp32, topk_idx [T, K] int32 (from moe_route); losses [2] fp32 out:
+ *   {L_dev, L_comm}.
+ */
+moe_status moe_group_balance_losses(const moe_config* cfg, int32_t T, const float* logits,
+                                    const int32_t* topk_idx, float* losses, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Sequence-wise balance loss ([P3] DeepSeek-v3, "sequence粒度的负载均衡loss"): the expert-level
  * balance loss of moe_load_stats computed within each sequence instead of over the batch, and
  * averaged over the sequences. The page gives no formula; this is the plain reading:
@@ -265,6 +281,33 @@ moe_status moe_get_error(moe_stream_t stream);
  * gives up, records MOE_ERR_TIMEOUT in the device error word and the kernel returns; read it
  * with moe_get_error(). No fault, no trap, the context stays usable. */
 moe_status moe_selftest_wait_timeout(int32_t timeout_us, moe_stream_t stream);
+
+/*
+ * Redundant-expert placement planner (host only, no GPU; [P4] sections 2 and 4: replicate hot
+ * experts, place the replicas on the GPUs of an expert-parallel deployment). From each expert's
+ * measured load (e.g. moe_load_stats counts summed over a serving window):
+ *   replicate: the n_gpus * slots_per_gpu - n_experts extra replicas go, one at a time, to the
+ *     expert with the largest load per replica (ties: lower expert) among the experts with fewer
+ *     replicas than there are GPUs (while any remains); a replica carries load / replicas;
+ *   place: replicas by decreasing load (ties: lower expert, lower replica) onto the least-loaded
+ *     GPU with a free slot that does not host that expert yet (ties: lower GPU), else onto the
+ *     least-loaded GPU with a free slot;
+ *   n_nodes > 1 (hierarchical, [P4] section 2): expert groups (n_groups of consecutive experts)
+ *     first go, heaviest first, to the least-loaded node with room (n_groups / n_nodes groups
+ *     per node); then each node replicates and places its own experts on its n_gpus / n_nodes
+ *     GPUs (GPU g is on node g / (n_gpus / n_nodes)).
+ *   load [n_experts] (>= 0); replicas [n_experts] out; gpu_expert [n_gpus * slots_per_gpu] out:
+ *   the experts each GPU hosts (-1 = empty slot); gpu_load [n_gpus] out (may be NULL).
+ */
+typedef struct {
+  int32_t n_experts;
+  int32_t n_gpus;
+  int32_t slots_per_gpu;
+  int32_t n_nodes;   /* <= 1: global placement */
+  int32_t n_groups;  /* hierarchical placement only */
+} moe_placement_config;
+moe_status moe_plan_placement(const moe_placement_config* pc, const int64_t* load,
+                              int32_t* replicas, int32_t* gpu_expert, double* gpu_load);
 
 /* Number of kernels this library has launched in this process so far (all devices, all
  * streams; a launch made while a stream is captured into a CUDA graph counts once, at capture).

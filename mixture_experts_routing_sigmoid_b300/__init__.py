@@ -16,7 +16,8 @@ __all__ = ["MoeError", "MoeConfig", "MoeWeights", "lib", "make_config", "make_we
            "moe_expert_ffn", "moe_expert_up", "moe_expert_down", "moe_combine",
            "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
            "moe_status_string", "moe_permute_static_scratch", "moe_stage_timing_start",
-           "moe_stage_timing_stop", "moe_bias_update", "moe_seq_balance_loss", "moe_kernel_launches", "STAGE_NAMES", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
+           "moe_stage_timing_stop", "moe_bias_update", "moe_seq_balance_loss", "moe_kernel_launches", "moe_group_balance_losses",
+           "moe_plan_placement", "MoePlacementConfig", "STAGE_NAMES", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
            "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT",
            "MOE_ERR_DEVICE_CHECK"]
 
@@ -32,7 +33,8 @@ EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_load_stats", "moe_pe
                     "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
                     "moe_status_string", "moe_last_error_detail", "moe_permute_static_scratch",
                     "moe_stage_timing_start", "moe_stage_timing_stop", "moe_bias_update",
-                    "moe_seq_balance_loss", "moe_kernel_launches")
+                    "moe_seq_balance_loss", "moe_kernel_launches", "moe_group_balance_losses",
+                    "moe_plan_placement")
 
 # Stages of moe_layer_forward as moe_stage_timing_stop reports them (MOE_N_STAGES).
 STAGE_NAMES = ("gate", "route", "stats", "permute", "dispatch", "up", "down", "combine")
@@ -61,6 +63,12 @@ class MoeWeights(ctypes.Structure):
                 ("w2_shared", ctypes.c_void_p)]
 
 
+class MoePlacementConfig(ctypes.Structure):
+    _fields_ = [("n_experts", ctypes.c_int32), ("n_gpus", ctypes.c_int32),
+                ("slots_per_gpu", ctypes.c_int32), ("n_nodes", ctypes.c_int32),
+                ("n_groups", ctypes.c_int32)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
@@ -87,6 +95,8 @@ def _load():
         "moe_bias_update": (I32, [CFG, P, ctypes.c_float, P, P]),
         "moe_seq_balance_loss": (I32, [CFG, I32, I32, P, P, P, P, P, SZ, P]),
         "moe_kernel_launches": (ctypes.c_ulonglong, []),
+        "moe_group_balance_losses": (I32, [CFG, I32, P, P, P, P, SZ, P]),
+        "moe_plan_placement": (I32, [ctypes.POINTER(MoePlacementConfig), P, P, P, P]),
         "moe_stage_timing_stop": (I32, [P, I32, P]),
     }
     for name, (res, args) in sig.items():
@@ -269,3 +279,26 @@ def moe_seq_balance_loss(cfg, T, seq_len, logits, topk_idx, per_seq, loss, ws, s
 def moe_kernel_launches() -> int:
     """Kernels launched by the library so far (a graph-captured launch counts once)."""
     return int(lib.moe_kernel_launches())
+
+
+def moe_group_balance_losses(cfg, T, logits, topk_idx, losses, ws, stream=None):
+    p, n = _ws(ws)
+    _check(lib.moe_group_balance_losses(ctypes.byref(_cfg(cfg)), int(T), _ptr(logits),
+                                        _ptr(topk_idx), _ptr(losses), p, n, _stream(stream)),
+           "moe_group_balance_losses")
+
+
+def moe_plan_placement(load, n_gpus: int, slots_per_gpu: int, n_nodes: int = 1,
+                       n_groups: int = 0):
+    """Host-only planner. load: sequence of per-expert loads (int). -> (replicas [N] int32,
+    gpu_expert [n_gpus, slots] int32 (-1 = empty), gpu_load [n_gpus] float64) as numpy."""
+    import numpy as np
+    ld = np.ascontiguousarray(np.asarray(load, dtype=np.int64))
+    N = int(ld.size)
+    pc = MoePlacementConfig(N, int(n_gpus), int(slots_per_gpu), int(n_nodes), int(n_groups))
+    reps = np.zeros(N, np.int32)
+    ge = np.zeros((int(n_gpus), int(slots_per_gpu)), np.int32)
+    gl = np.zeros(int(n_gpus), np.float64)
+    _check(lib.moe_plan_placement(ctypes.byref(pc), ld.ctypes.data, reps.ctypes.data,
+                                  ge.ctypes.data, gl.ctypes.data), "moe_plan_placement")
+    return reps, ge, gl

@@ -103,7 +103,7 @@ size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 // Workspace carve for one config and token count. Every region is 256-byte aligned.
 struct Layout {
   size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_lse,
-      counts, seq_s, seq_c, seq_lb, gate_part, xy_perm, h, h_sh, y_sh, total;
+      counts, recv, seq_s, seq_c, seq_lb, gate_part, xy_perm, h, h_sh, y_sh, total;
 };
 
 Layout layout(const moe_config* c, int32_t T) {
@@ -129,6 +129,7 @@ Layout layout(const moe_config* c, int32_t T) {
   L.part_s = take(nbs * N * 4);
   L.part_lse = take(nbs * 2 * 8);
   L.counts = take(N * 4);
+  L.recv = take(32 * 4);
   // sequence-wise loss: B * chunks <= T / 64 + B <= T + T / 64 partial rows for any seq_len
   const size_t seq_rows = Tt + Tt / 64 + 1;
   L.seq_s = take(seq_rows * N * 4);
@@ -562,6 +563,32 @@ moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float r
   a.rate = rate;
   a.bias = select_bias;
   return cuda_status(launch_bias_update(a, S_(stream)), "bias update");
+}
+
+moe_status moe_group_balance_losses(const moe_config* cfg, int32_t T, const float* logits,
+                                    const int32_t* topk_idx, float* losses, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream) {
+  g_detail[0] = 0;
+  TRY(check_cfg(cfg, T));
+  if (T == 0) return fail(MOE_ERR_INVALID_ARG, "the group losses need T > 0");
+  CHECK_PTR(logits);
+  CHECK_PTR(topk_idx);
+  CHECK_PTR(losses);
+  TRY(check_ws(cfg, T, ws, ws_bytes));
+  const Layout L = layout(cfg, T);
+  GroupLossArgs a;
+  a.st.T = T; a.st.N = cfg->n_routed; a.st.K = cfg->top_k; a.st.score_fn = cfg->score_fn;
+  a.st.u = logits; a.st.idx = topk_idx;
+  a.st.counts = at<int32_t>(ws, L.counts);
+  a.st.f = nullptr; a.st.P = nullptr; a.st.lb_z = nullptr;
+  a.st.part_s = at<float>(ws, L.part_s);
+  a.st.part_lse = at<double>(ws, L.part_lse);
+  a.st.nblk = stats_blocks(T);
+  a.st.err = error_word();
+  a.G = cfg->n_groups;
+  a.recv = at<int32_t>(ws, L.recv);
+  a.out = losses;
+  return cuda_status(launch_group_losses(a, S_(stream)), "group balance losses");
 }
 
 moe_status moe_seq_balance_loss(const moe_config* cfg, int32_t T, int32_t seq_len,

@@ -38,6 +38,15 @@ struct StatsArgs {
 int stats_blocks(int T);
 cudaError_t launch_stats(const StatsArgs& a, cudaStream_t st);
 
+// Device-level and communication balance losses over the n_groups devices (route.cu).
+struct GroupLossArgs {
+  StatsArgs st;         // logits, idx, counts scratch, score partials (lb_z, f, P unused)
+  int G;
+  int32_t* recv;        // scratch [G]: tokens each device receives
+  float* out;           // [2]: L_dev, L_comm
+};
+cudaError_t launch_group_losses(const GroupLossArgs& a, cudaStream_t st);
+
 // ---------------------------------------------------------------- balancing (balance.cu)
 struct BiasUpdateArgs {
   int N;

@@ -424,7 +424,75 @@ __global__ void __launch_bounds__(256) stats_final_kernel(StatsArgs a) {
   }
 }
 
+// Per token: expert counts, and one received token for each distinct device it uses.
+__global__ void group_count_kernel(GroupLossArgs a) {
+  const int per = a.st.N / a.G;
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < a.st.T; t += gridDim.x * blockDim.x) {
+    uint32_t devs = 0;
+    for (int k = 0; k < a.st.K; ++k) {
+      const int e = a.st.idx[(size_t)t * a.st.K + k];
+      if (e < 0 || e >= a.st.N) { set_error(a.st.err, ERR_DEVICE_CHECK); continue; }
+      atomicAdd(&a.st.counts[e], 1);
+      devs |= 1u << (e / per);
+    }
+    while (devs) {
+      const int d = __ffs(devs) - 1;
+      devs &= devs - 1;
+      atomicAdd(&a.recv[d], 1);
+    }
+  }
+}
+
+// Fixed-order fp64 reduction: per-expert score sums and counts -> per-device shares -> losses.
+__global__ void __launch_bounds__(256) group_final_kernel(GroupLossArgs a) {
+  __shared__ double colsum[256];
+  __shared__ double tot[1];
+  const int e = threadIdx.x, N = a.st.N;
+  double cs = 0.0;
+  if (e < N)
+    for (int b = 0; b < a.st.nblk; ++b) cs += (double)a.st.part_s[(size_t)b * N + e];
+  colsum[e] = cs;
+  __syncthreads();
+  if (e == 0) {
+    double t = 0.0;
+    for (int i = 0; i < N; ++i) t += colsum[i];
+    tot[0] = t;
+  }
+  __syncthreads();
+  if (e == 0) {
+    const int per = N / a.G;
+    double recv_tot = 0.0;
+    for (int d = 0; d < a.G; ++d) recv_tot += (double)a.recv[d];
+    double l_dev = 0.0, l_comm = 0.0;
+    for (int d = 0; d < a.G; ++d) {
+      double f = 0.0, P = 0.0;
+      for (int i = d * per; i < (d + 1) * per; ++i) {
+        f += (double)a.st.counts[i] / ((double)a.st.T * a.st.K);
+        P += colsum[i] / tot[0];
+      }
+      l_dev += f * P;
+      l_comm += (double)a.recv[d] / recv_tot * P;
+    }
+    a.out[0] = (float)(a.G * l_dev);
+    a.out[1] = (float)(a.G * l_comm);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_group_losses(const GroupLossArgs& a, cudaStream_t st) {
+  if (a.st.T <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(a.st.counts, 0, sizeof(int32_t) * a.st.N, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.recv, 0, sizeof(int32_t) * a.G, st);
+  if (e != cudaSuccess) return e;
+  int cb = (a.st.T + 255) / 256;
+  if (cb > 1184) cb = 1184;
+  group_count_kernel<<<cb, 256, 0, st>>>(a);
+  stats_partial_kernel<<<a.st.nblk, 256, 0, st>>>(a.st);
+  group_final_kernel<<<1, 256, 0, st>>>(a);
+  note_launches(3);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;

@@ -145,6 +145,36 @@ def seq_balance_loss(cfg, u, s, idx, seq_len: int):
     return per, float(per.mean())
 
 
+def group_balance_losses(cfg, u, s, idx):
+    """Device-level and communication balance losses ("DeepSeek MoE：从v1到v3的演进",
+    DeepSeek-v1 设备级负载loss and DeepSeek-v2 通信负载均衡loss). The page describes them in words
+    only; the reading taken follows the expert-level loss of the ST-MoE section with the
+    n_groups devices (expert e on device e / (N / G)) as the units:
+      f'_d = sum over e on d of f_e   (share of the batch's assignments d computes),
+      P'_d = sum over e on d of P_e   (share of the router score d receives),
+      L_dev = G * sum_d f'_d P'_d;
+      R_d  = number of tokens with at least one chosen expert on d (tokens d receives),
+      f''_d = R_d / sum_d' R_d',  L_comm = G * sum_d f''_d P'_d.
+    Both are 1 when routing is uniform. -> (L_dev, L_comm)."""
+    st = load_stats(cfg, u, s, idx)
+    G, N = cfg.n_groups, cfg.n_routed
+    per = N // G
+    dev_of = np.arange(N) // per
+    f_dev = np.zeros(G)
+    p_dev = np.zeros(G)
+    for e in range(N):
+        f_dev[dev_of[e]] += st.f[e]
+        p_dev[dev_of[e]] += st.P[e]
+    recv = np.zeros(G)
+    idx = np.asarray(idx)
+    for t in range(idx.shape[0]):
+        for d in sorted(set(int(e) // per for e in idx[t])):
+            recv[d] += 1
+    l_dev = G * float(np.sum(f_dev * p_dev))
+    l_comm = G * float(np.sum(recv / recv.sum() * p_dev))
+    return l_dev, l_comm
+
+
 def capacity_drop(cfg, idx, w) -> np.ndarray:
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     w = _f64(w)
@@ -284,3 +314,67 @@ def layer_forward(cfg, x, w_gate, gate_bias, select_bias, expert_weights, shared
     res["tokens"] = all_tokens
     res["out"] = combine(y_rows, slot, w_o, y_sh)
     return res
+
+
+# ---------------------------------------------------------------- expert placement planner
+def plan_placement(load, n_gpus: int, slots: int, n_nodes: int = 1, n_groups: int = 0):
+    """Redundant-expert placement ("DeepSeek-V3的Group-Limited Expert Routing与负载均衡优化实践",
+    sections 2 and 4: give hot experts replicas, place replicas on GPUs; hierarchically for
+    prefill: expert groups to nodes first). The pages name the steps; the rules taken:
+      replicate: one extra replica at a time to the expert with the largest load per replica
+        (ties: lower expert), among experts with fewer replicas than GPUs while any remains;
+      place: replicas by decreasing load per replica (ties: lower expert, lower replica) onto the
+        least-loaded GPU with a free slot not yet hosting that expert (ties: lower GPU), else
+        onto the least-loaded GPU with a free slot;
+      groups (n_nodes > 1): by decreasing load (ties: lower group) onto the least-loaded node
+        with room for one more group.
+    Plain loops, fractions for the replication comparisons.
+    -> (replicas [N], gpu_expert [n_gpus][slots] with -1 for empty slots, gpu_load [n_gpus])."""
+    from fractions import Fraction
+    load = [int(v) for v in load]
+    N = len(load)
+    reps = [0] * N
+    hosted = [[] for _ in range(n_gpus)]
+    gload = [0.0] * n_gpus
+
+    def replicate(ids, total, cap):
+        for e in ids:
+            reps[e] = 1
+        for _ in range(total - len(ids)):
+            below = [e for e in ids if reps[e] < cap]
+            cand = below if below else list(ids)
+            best = max(cand, key=lambda e: (Fraction(load[e], reps[e]), -e))
+            reps[best] += 1
+
+    def place(ids, gpus):
+        items = [(load[e] / reps[e], e, j) for e in ids for j in range(reps[e])]
+        items.sort(key=lambda it: (-it[0], it[1], it[2]))
+        for w, e, _ in items:
+            free = [g for g in gpus if len(hosted[g]) < slots]
+            fresh = [g for g in free if e not in hosted[g]]
+            pool = fresh if fresh else free
+            g = min(pool, key=lambda g: (gload[g], g))
+            hosted[g].append(e)
+            gload[g] += w
+
+    if n_nodes <= 1:
+        replicate(list(range(N)), n_gpus * slots, n_gpus)
+        place(list(range(N)), list(range(n_gpus)))
+    else:
+        gpn, per, gpnode = n_gpus // n_nodes, N // n_groups, n_groups // n_nodes
+        gl = [sum(load[g * per:(g + 1) * per]) for g in range(n_groups)]
+        order = sorted(range(n_groups), key=lambda g: (-gl[g], g))
+        nl, nc, node_groups = [0] * n_nodes, [0] * n_nodes, [[] for _ in range(n_nodes)]
+        for g in order:
+            n = min((n for n in range(n_nodes) if nc[n] < gpnode), key=lambda n: (nl[n], n))
+            node_groups[n].append(g)
+            nc[n] += 1
+            nl[n] += gl[g]
+        for n in range(n_nodes):
+            ids = [e for g in sorted(node_groups[n]) for e in range(g * per, (g + 1) * per)]
+            replicate(ids, gpn * slots, gpn)
+            place(ids, list(range(n * gpn, (n + 1) * gpn)))
+    ge = np.full((n_gpus, slots), -1, np.int32)
+    for g in range(n_gpus):
+        ge[g, :len(hosted[g])] = hosted[g]
+    return np.array(reps, np.int32), ge, np.array(gload, np.float64)

@@ -95,3 +95,25 @@ def test_seq_balance_loss_rejects_bad_seq_len():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_seq_balance_loss(cfg, cfg.T, 7, u, idx, None, loss, workspace(cfg, cfg.T))
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["tiny", "v2", "v3_prefill", "v3_decode_512"])
+def test_group_balance_losses_match_oracle(name):
+    """Device-level and communication losses on identical logits and routing: within 1e-5
+    relative of the fp64 oracle (fp32 score sums)."""
+    import mixture_experts_routing_sigmoid_b300 as moe
+    from moe_inputs import make_logits, make_router
+    from tests.helpers import gpu_route, workspace
+    cfg = CONFIGS[name]
+    T = cfg.T
+    u = make_logits(cfg, seed=13, T=T)
+    sb = make_router(cfg)["select_bias"]
+    idx, _, _ = gpu_route(cfg, T, logits=u.cuda(),
+                          weights={"select_bias": None if sb is None else sb.cuda()})
+    out = torch.empty(2, dtype=torch.float32, device="cuda")
+    moe.moe_group_balance_losses(cfg, T, u.cuda(), idx, out, workspace(cfg, T))
+    assert moe.moe_get_error() == 0
+    ud = u.double().numpy()
+    want = oracle.group_balance_losses(cfg, ud, oracle.scores(ud, cfg.score_fn),
+                                       idx.cpu().numpy())
+    np.testing.assert_allclose(out.cpu().numpy(), want, rtol=1e-5)

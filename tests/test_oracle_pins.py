@@ -436,3 +436,50 @@ def test_seq_balance_sees_imbalance_the_batch_loss_hides():
     per, mean = oracle.seq_balance_loss(cfg, u, s, idx, L)
     np.testing.assert_allclose(per, N / K, rtol=1e-12)
     assert abs(oracle.load_stats(cfg, u, s, idx).lb - 1.0) < 1e-12
+
+
+# ------------------------------------------------------------------ device / communication losses
+def _route(cfg, u, sb=None):
+    s = oracle.scores(u, cfg.score_fn)
+    idx, _, _ = oracle.route(cfg, s, sb)
+    return s, idx
+
+
+def test_group_losses_one_expert_per_device_is_expert_loss():
+    """With as many devices as experts, the device-level loss is the expert-level L_B."""
+    cfg = CONFIGS["v1"].replace(T=128, n_routed=16, top_k=4, n_groups=16, topk_groups=16)
+    u = np.random.default_rng(8).normal(0, 1, (cfg.T, 16))
+    s, idx = _route(cfg, u)
+    l_dev, _ = oracle.group_balance_losses(cfg, u, s, idx)
+    assert abs(l_dev - oracle.load_stats(cfg, u, s, idx).lb) < 1e-12
+
+
+def test_group_losses_top1_communication_equals_device_loss():
+    """With one expert per token each token reaches exactly one device, so the received-token
+    shares equal the assignment shares and the two losses coincide."""
+    cfg = CONFIGS["v1"].replace(T=200, n_routed=16, top_k=1, n_groups=4, topk_groups=4)
+    u = np.random.default_rng(9).normal(0, 1, (cfg.T, 16))
+    s, idx = _route(cfg, u)
+    l_dev, l_comm = oracle.group_balance_losses(cfg, u, s, idx)
+    assert abs(l_dev - l_comm) < 1e-12
+
+
+def test_group_losses_uniform_routing_gives_one():
+    N, K, G = 16, 4, 4
+    cfg = CONFIGS["v1"].replace(T=64, n_routed=N, top_k=K, n_groups=G, topk_groups=G)
+    u = _uniform_stats_inputs(N, K, cfg.T)
+    s, idx = _route(cfg, u)
+    l_dev, l_comm = oracle.group_balance_losses(cfg, u, s, idx)
+    assert abs(l_dev - 1.0) < 1e-12 and abs(l_comm - 1.0) < 1e-12
+
+
+def test_group_losses_collapse_onto_one_device():
+    """Every token sends all its assignments and (almost) all its score to device 0: both losses
+    approach G, the number of devices."""
+    N, K, G = 16, 4, 4
+    cfg = CONFIGS["v1"].replace(T=32, n_routed=N, top_k=K, n_groups=G, topk_groups=G)
+    u = np.full((cfg.T, N), -60.0)
+    u[:, :4] = 0.0
+    s, idx = _route(cfg, u)
+    l_dev, l_comm = oracle.group_balance_losses(cfg, u, s, idx)
+    np.testing.assert_allclose([l_dev, l_comm], [G, G], rtol=1e-12)
