@@ -103,7 +103,7 @@ size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 // Workspace carve for one config and token count. Every region is 256-byte aligned.
 struct Layout {
   size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_lse,
-      counts, recv, seq_s, seq_c, seq_lb, gate_part, xy_perm, h, h_sh, y_sh, total;
+      counts, recv, seq_s, seq_c, seq_lb, gate_part, sched, xy_perm, h, h_sh, y_sh, total;
 };
 
 Layout layout(const moe_config* c, int32_t T) {
@@ -136,6 +136,7 @@ Layout layout(const moe_config* c, int32_t T) {
   L.seq_c = take(seq_rows * N * 4);
   L.seq_lb = take(Tt * 8);
   L.gate_part = take((size_t)GATE_PART_ROWS * N * 4);
+  L.sched = take(2 * 4);          // tile counters of the up and down GEMMs
   L.xy_perm = take(A * H * eb);   // x_perm, then reused for y_perm
   L.h = take(A * I * eb);
   L.h_sh = take(Tt * (S > 0 ? S : 1) * I * eb);
@@ -274,8 +275,17 @@ moe_status do_permute(const moe_config* c, int32_t T, const int32_t* idx, const 
   return cuda_status(launch_dispatch(p, num_sms(), st), "row dispatch");
 }
 
+// Zero the up and down GEMMs' tile counters in the workspace (one memset node per FFN).
+moe_status reset_sched(const moe_config* c, int32_t T, void* ws, cudaStream_t st) {
+  if (c->dtype != MOE_BF16) return MOE_OK;
+  return cuda_status(cudaMemsetAsync(at<int32_t>(ws, layout(c, T).sched), 0, 2 * sizeof(int32_t), st),
+                     "tile counter reset");
+}
+
+// sched: the two tile counters (up, down) zeroed by reset_sched, or nullptr (static schedule).
 moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32_t* offsets,
-                 const void* x, const moe_weights* w, void* h, void* h_sh, cudaStream_t st) {
+                 const void* x, const moe_weights* w, void* h, void* h_sh, int32_t* sched,
+                 cudaStream_t st) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_UP;
@@ -284,12 +294,14 @@ moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32
   g.offsets = offsets; g.rows_cap = T * c->top_k;
   g.a0 = x_perm; g.a1 = x; g.b0 = w->w13; g.b1 = w->w13_shared;
   g.out0 = h; g.out1 = h_sh; g.err = error_word();
+  g.sched = sched;
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "expert up GEMM");
 }
 
 moe_status do_down(const moe_config* c, int32_t T, const void* h, const int32_t* offsets,
-                   const void* h_sh, const moe_weights* w, void* y, void* y_sh, cudaStream_t st) {
+                   const void* h_sh, const moe_weights* w, void* y, void* y_sh, int32_t* sched,
+                   cudaStream_t st) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_DOWN;
@@ -298,6 +310,7 @@ moe_status do_down(const moe_config* c, int32_t T, const void* h, const int32_t*
   g.offsets = offsets; g.rows_cap = T * c->top_k;
   g.a0 = h; g.a1 = h_sh; g.b0 = w->w2; g.b1 = w->w2_shared;
   g.out0 = y; g.out1 = y_sh; g.err = error_word();
+  g.sched = sched ? sched + 1 : nullptr;
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "expert down GEMM");
 }
@@ -357,10 +370,12 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
     TRY(do_stats(cfg, T, u, idx, counts, nullptr, nullptr, lb_z, ws, st));
   stage_mark(STAGE_PERMUTE, st);
   TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, slot_row, xy, ws, st));
+  int32_t* sched = at<int32_t>(ws, L.sched);
   stage_mark(STAGE_UP, st);
-  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, st));
+  TRY(reset_sched(cfg, T, ws, st));
+  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, sched, st));
   stage_mark(STAGE_DOWN, st);
-  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, st));  // y_perm overwrites x_perm
+  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, sched, st));  // y_perm overwrites x_perm
   stage_mark(STAGE_COMBINE, st);
   return do_combine(cfg, T, xy, slot_row, wt, y_sh, out, st);
 }
@@ -470,7 +485,7 @@ moe_status moe_expert_up(const moe_config* cfg, int32_t T, const void* x_perm,
     CHECK_PTR(x);
     CHECK_PTR(h_shared);
   }
-  return do_up(cfg, T, x_perm, offsets, x, w, h, h_shared, S_(stream));
+  return do_up(cfg, T, x_perm, offsets, x, w, h, h_shared, nullptr, S_(stream));
 }
 
 moe_status moe_expert_down(const moe_config* cfg, int32_t T, const void* h,
@@ -487,7 +502,7 @@ moe_status moe_expert_down(const moe_config* cfg, int32_t T, const void* h,
     CHECK_PTR(h_shared);
     CHECK_PTR(y_shared);
   }
-  return do_down(cfg, T, h, offsets, h_shared, w, y_perm, y_shared, S_(stream));
+  return do_down(cfg, T, h, offsets, h_shared, w, y_perm, y_shared, nullptr, S_(stream));
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const void* x_perm,
@@ -509,8 +524,10 @@ moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const void* x_perm,
   const Layout L = layout(cfg, T);
   void* h = at<char>(ws, L.h);
   void* h_sh = cfg->n_shared > 0 ? at<char>(ws, L.h_sh) : nullptr;
-  TRY(do_up(cfg, T, x_perm, offsets, x, w, h, h_sh, S_(stream)));
-  return do_down(cfg, T, h, offsets, h_sh, w, y_perm, y_shared, S_(stream));
+  int32_t* sched = at<int32_t>(ws, L.sched);
+  TRY(reset_sched(cfg, T, ws, S_(stream)));
+  TRY(do_up(cfg, T, x_perm, offsets, x, w, h, h_sh, sched, S_(stream)));
+  return do_down(cfg, T, h, offsets, h_sh, w, y_perm, y_shared, sched, S_(stream));
 }
 
 moe_status moe_combine(const moe_config* cfg, int32_t T, const void* y_perm,

@@ -107,26 +107,37 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                :: "r"(bar), "r"(bytes) : "memory");
 }
+// CLUSTER: acquire at cluster scope, for phases completed by arrivals of the other CTA of the
+// cluster that publish data it wrote (or order its reads before ours).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  if (CLUSTER)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
 
 // Bounded wait on an mbarrier phase, polled by the calling thread. Returns false (and raises
 // the CTA's abort flag and the device error word) once `timeout_ns` has passed, or as soon as
 // another thread of the CTA has raised the abort flag. Never traps, never spins forever.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int* err,
                                                   unsigned long long timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > timeout_ns) {
@@ -139,11 +150,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // Warp-uniform version: lane 0 polls, the outcome is broadcast to the warp.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int* err,
                                                   unsigned long long timeout_ns) {
   int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort_flag, err, timeout_ns);
+  if ((threadIdx.x & 31) == 0)
+    ok = mbar_wait_bounded<CLUSTER>(bar, parity, abort_flag, err, timeout_ns);
   ok = __shfl_sync(FULL_MASK, ok, 0);
   __syncwarp();
   return ok != 0;
@@ -241,6 +254,10 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
+}
+// 32-bit store to shared memory of a CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");
 }
 // Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {

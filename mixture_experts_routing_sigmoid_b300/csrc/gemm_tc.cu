@@ -33,12 +33,15 @@
 // problem by problem, weight tile by weight tile, token tile fastest (a segment's rows are
 // split into equal token tiles), so the pairs running together share weight tiles in L2.
 //   warp 0      TMA producer (both CTAs): this CTA's weight rows and token rows of one k block
-//               (64 elements) per stage, 128-byte swizzle, 6-stage ring of 32 KB stages.
+//               per stage, 3-stage ring of 64 KB stages. A k block is 128 elements, two
+//               128-byte-swizzled units of 64 (one TMA box per operand and unit); when K / 64 is
+//               odd the last block holds one unit. Fewer, larger stages halve the barrier
+//               round trips per FLOP at the same bytes in flight.
 //               Completion of both CTAs' loads is counted on the first CTA's full barrier; the
 //               MMA's commit frees the stage in both CTAs.
 //   warp 1      TMEM owner (both CTAs) and, in the first CTA, MMA issuer: a single thread waits
-//               for each stage and issues its four tcgen05.mma (M=256, N=tile's tokens rounded
-//               up to 16, K=16) into one of two 256-column fp32 accumulators.
+//               for each stage and issues its tcgen05.mma (M=256, N=tile's tokens rounded up to
+//               16, K=16; four per unit) into one of two 256-column fp32 accumulators.
 //   warps 2..5  epilogue (both CTAs): tcgen05.ld of the warp's 32 TMEM lanes, SwiGLU / router
 //               bias, stores.
 // Token columns past the segment end belong to the next expert (or lie beyond the tensor,
@@ -55,9 +58,10 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;                  // weight rows per CTA and operand (MMA M = 256)
-constexpr int BK = 64;                   // reduction elements per stage (128 bytes of bf16)
+constexpr int KU = 64;                   // reduction elements per unit (128 bytes of bf16)
+constexpr int UNITS = 2;                 // units per stage (k block of 128 elements)
 constexpr int MAXP = 258;
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;       // two accumulators
 constexpr int XBOX_S = 32, XBOX_L = 64;  // token rows per TMA box (small / large map)
@@ -65,9 +69,12 @@ constexpr unsigned long long TIMEOUT_NS = 2000000000ull;    // 2 s per wait
 constexpr unsigned long long GRACE_NS = 100000000ull;       // drain after an abort
 
 constexpr int TOK = 256;                 // tokens per tile at most (MMA N)
-constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * BK * 2;     // this CTA's weight rows
-constexpr int B_BYTES = TOK / 2 * BK * 2;  // this CTA's token rows (at most)
+constexpr int STAGES = 3;
+constexpr int SQ = 4;                    // tile schedule ring slots
+constexpr int A_UNIT = BM * KU * 2;      // this CTA's weight rows, one unit
+constexpr int B_UNIT = TOK / 2 * KU * 2;  // this CTA's token rows (at most), one unit
+constexpr int A_BYTES = UNITS * A_UNIT;
+constexpr int B_BYTES = UNITS * B_UNIT;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 
 struct TcParams {
@@ -80,9 +87,29 @@ struct TcParams {
   void* out1;
   const float* gate_bias;
   float* gate_part;          // GATE split-K: partial sums [splits][T][N]
-  int splits, kb_per_split;  // GATE: K range split over `splits` tiles (1 = no split)
+  int* sched;                // tile counter (zero at launch) for the dynamic schedule, or null
+  int splits, ku_per_split;  // GATE: K range split over `splits` tiles (1 = no split); units
+                             // per split, even
   int* err;
 };
+
+// One tile, as decoded by the first CTA's producer and passed to every other role through the
+// schedule rings (words only: it travels as three 16-byte vectors).
+struct alignas(16) Tile {
+  int prob;      // problem index; -1: no more tiles
+  int f0;        // first output feature of the tile; this CTA's are f0 + feat_per_cta * rank ..
+  int r0;        // first token row (in the problem's activation tensor)
+  int nrows;     // token rows of this tile that are stored
+  int ncols;     // MMA N: nrows rounded up to 16; each CTA holds ncols / 2 token rows
+  int nbox;      // token boxes loaded per CTA and stage
+  int big_box;   // boxes of 64 rows (else one box of 32)
+  int ku0, ku;   // first k unit and k units (GATE split-K: this split's range)
+  int kb;        // k blocks (stages): ku / UNITS rounded up
+  int split;     // GATE split-K: which split
+  int shared;    // the shared experts' problem
+};
+constexpr int TILE_WORDS = sizeof(Tile) / 4;
+static_assert(TILE_WORDS == 12, "a tile travels as three 16-byte vectors");
 
 struct SmemCtl {
   uint64_t full[STAGES];       // first CTA's copy counts both CTAs' loads
@@ -90,13 +117,23 @@ struct SmemCtl {
   uint64_t tfull[2];           // per CTA, arrived on by the MMA commit
   uint64_t tempty[2];          // first CTA's copy: 4 epilogue warps x 2 CTAs
   uint64_t drain;
+  // tile schedule: a CTA-local ring in each CTA (written by the CTA's producer, read by its
+  // MMA issuer and epilogue warps) and a channel from the first CTA's producer to the second's
+  uint64_t lfull[SQ];          // lsq[slot] holds the next tile
+  uint64_t lempty[SQ];         // the slot's local readers are done with it
+  uint64_t xfull[SQ];          // second CTA: xq[slot] arrived (tx-counted, 48 bytes)
+  uint64_t xempty[SQ];         // first CTA: the second CTA's scheduler has read xq[slot]
+  uint64_t took;               // first CTA: its producer has started the last published tile
+  Tile lsq[SQ];
+  Tile xq[SQ];
   uint32_t tmem_base;
   int abort_flag;
   int nprob;
   int total_tiles;
   int tile_start[MAXP + 1];   // by position in `order`
   int order[MAXP];            // problems, most rows first (ties: lower index)
-  int rows[MAXP];
+  int rows[MAXP];             // by problem: rows and first row of its segment
+  int row0[MAXP];
 };
 
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
@@ -117,23 +154,10 @@ __device__ __forceinline__ int n_feat_tiles(const TcParams& p, bool shared) {
   return (feat_total<MODE>(p, shared) + 2 * feat_per_cta<MODE>() - 1) / (2 * feat_per_cta<MODE>());
 }
 template <int MODE>
-__device__ __forceinline__ int k_blocks_of(const TcParams& p, bool shared) {
-  if (MODE == MODE_DOWN) return (shared ? p.S * p.I : p.I) / BK;
-  return p.H / BK;
+__device__ __forceinline__ int k_units_of(const TcParams& p, bool shared) {
+  if (MODE == MODE_DOWN) return (shared ? p.S * p.I : p.I) / KU;
+  return p.H / KU;
 }
-
-struct Tile {
-  int prob;      // problem index
-  int f0;        // first output feature of the tile; this CTA's are f0 + feat_per_cta * rank ..
-  int r0;        // first token row (in the problem's activation tensor)
-  int nrows;     // token rows of this tile that are stored
-  int ncols;     // MMA N: nrows rounded up to 16; each CTA holds ncols / 2 token rows
-  int nbox;      // token boxes loaded per CTA and stage
-  bool big_box;  // boxes of 64 rows (else one box of 32)
-  int kb0, kb;   // first k block and k blocks (GATE split-K: this split's range)
-  int split;     // GATE split-K: which split
-  bool shared;
-};
 
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c, int tile) {
@@ -147,11 +171,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   lo = c.order[pos];
   t.prob = lo;
   t.shared = (MODE != MODE_GATE) && lo >= p.n_routed;
-  int row0 = 0, rows = p.T;
-  if (MODE != MODE_GATE && !t.shared) {
-    row0 = __ldg(p.offsets + lo);
-    rows = __ldg(p.offsets + lo + 1) - row0;
-  }
+  const int row0 = c.row0[lo], rows = c.rows[lo];
   const int ntt = (rows + TOK - 1) / TOK;
   int local = tile - c.tile_start[pos];
   t.split = 0;
@@ -169,18 +189,28 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   t.nrows = min(per, rows - tt * per);
   t.ncols = (t.nrows + 15) & ~15;
   const int half = t.ncols / 2;
-  t.big_box = half > XBOX_S;
+  t.big_box = half > XBOX_S ? 1 : 0;
   t.nbox = t.big_box ? (half + XBOX_L - 1) / XBOX_L : 1;
-  t.kb0 = 0;
-  t.kb = k_blocks_of<MODE>(p, t.shared);
+  t.ku0 = 0;
+  t.ku = k_units_of<MODE>(p, t.shared);
   if (MODE == MODE_GATE && p.splits > 1) {
-    t.kb0 = t.split * p.kb_per_split;
-    t.kb = min(p.kb_per_split, t.kb - t.kb0);
+    t.ku0 = t.split * p.ku_per_split;
+    t.ku = min(p.ku_per_split, t.ku - t.ku0);
   }
+  t.kb = (t.ku + UNITS - 1) / UNITS;
   return t;
 }
 
-// Coordinates of this CTA's boxes for k block kb of tile t: the weight box at (ax, ay0) (UP:
+__device__ __forceinline__ Tile end_tile() {
+  Tile t;
+  int* w = reinterpret_cast<int*>(&t);
+#pragma unroll
+  for (int i = 0; i < TILE_WORDS; ++i) w[i] = 0;
+  t.prob = -1;
+  return t;
+}
+
+// Coordinates of this CTA's boxes for k unit ku of tile t: the weight box at (ax, ay0) (UP:
 // 5-D coordinates (ax, 0, 0, ay0 = first 16-feature group, ay1 = expert)); token boxes at
 // (bx, by0 + box_rows j), j < t.nbox.
 struct Boxes {
@@ -190,7 +220,7 @@ struct Boxes {
 };
 
 template <int MODE>
-__device__ __forceinline__ Boxes boxes_of(const TcParams& p, const Tile& t, int kb, uint32_t rank) {
+__device__ __forceinline__ Boxes boxes_of(const TcParams& p, const Tile& t, int ku, uint32_t rank) {
   Boxes b;
   b.tw = t.shared ? &p.tmW1 : &p.tmW0;
   if (t.big_box) {
@@ -200,8 +230,8 @@ __device__ __forceinline__ Boxes boxes_of(const TcParams& p, const Tile& t, int 
     b.tx = t.shared ? &p.tmX1s : &p.tmX0s;
     b.box_rows = XBOX_S;
   }
-  b.box_bytes = b.box_rows * BK * 2;
-  const int k0 = kb * BK;
+  b.box_bytes = b.box_rows * KU * 2;
+  const int k0 = ku * KU;
   b.ax = k0;
   b.ay1 = 0;
   int fc = t.f0 + (int)rank * feat_per_cta<MODE>();    // this CTA's first feature
@@ -261,6 +291,100 @@ __device__ __forceinline__ void store_bf16_chunk(const float (&v)[NT], __nv_bflo
   }
 }
 
+// ---- tile schedule: the first CTA's scheduler warp decides which tile the pair takes next,
+// decodes it and publishes it in its CTA's local ring and, with asynchronous remote stores that
+// count on a barrier of the second CTA (st.async), to the second CTA's scheduler warp, which
+// republishes it in its own local ring. The producer, MMA issuer and epilogue warps only read
+// their local ring: no wait on their path is cluster-scope, and no decoding sits between two
+// stages of a producer or MMA issuer.
+constexpr uint32_t LOCAL_READERS_0 = 6;  // first CTA: producer, MMA issuer, 4 epilogue warps
+constexpr uint32_t LOCAL_READERS_1 = 5;  // second CTA: producer, 4 epilogue warps
+constexpr uint32_t TILE_BYTES = sizeof(Tile);
+
+__device__ __forceinline__ void sts_tile(uint32_t a, const Tile& t) {
+  const int* w = reinterpret_cast<const int*>(&t);
+#pragma unroll
+  for (int i = 0; i < TILE_WORDS; i += 4)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(a + 4 * i), "r"(w[i]), "r"(w[i + 1]), "r"(w[i + 2]), "r"(w[i + 3]) : "memory");
+}
+__device__ __forceinline__ void lds_tile(uint32_t a, Tile& t) {
+  int* w = reinterpret_cast<int*>(&t);
+#pragma unroll
+  for (int i = 0; i < TILE_WORDS; i += 4)
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[i]), "=r"(w[i + 1]), "=r"(w[i + 2]), "=r"(w[i + 3]) : "r"(a + 4 * i) : "memory");
+}
+
+// Publish `t` in slot `qs` of this CTA's local ring. Warp-wide (producer warp).
+__device__ __forceinline__ bool ring_publish(SmemCtl& c, uint32_t qs, uint32_t qph, const Tile& t,
+                                             volatile int* abort_flag, int* err) {
+  if (!warp_wait_bounded(smem_u32(&c.lempty[qs]), qph ^ 1u, abort_flag, err, TIMEOUT_NS))
+    return false;
+  if ((threadIdx.x & 31) == 0) {
+    sts_tile(smem_u32(&c.lsq[qs]), t);
+    mbar_arrive(smem_u32(&c.lfull[qs]));
+  }
+  __syncwarp();
+  return true;
+}
+
+// First CTA: send `t` to slot `qs` of the second CTA's channel. Warp-wide (producer warp).
+__device__ __forceinline__ bool ring_send(SmemCtl& c, uint32_t qs, uint32_t qph, const Tile& t,
+                                          volatile int* abort_flag, int* err) {
+  if (!warp_wait_bounded(smem_u32(&c.xempty[qs]), qph ^ 1u, abort_flag, err, TIMEOUT_NS))
+    return false;
+  if ((threadIdx.x & 31) == 0) {
+    const int* w = reinterpret_cast<const int*>(&t);
+    const uint32_t dst = mapa_shared(smem_u32(&c.xq[qs]), 1);
+    const uint32_t rb = mapa_shared(smem_u32(&c.xfull[qs]), 1);
+#pragma unroll
+    for (int i = 0; i < TILE_WORDS; i += 4)
+      asm volatile(
+          "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+          :: "r"(dst + 4 * i), "r"(w[i]), "r"(w[i + 1]), "r"(w[i + 2]), "r"(w[i + 3]), "r"(rb)
+          : "memory");
+  }
+  __syncwarp();
+  return true;
+}
+
+// Second CTA: receive slot `qs` of the channel (warp-wide), re-arm its barrier for the next
+// use and hand the slot back to the first CTA.
+__device__ __forceinline__ bool ring_recv(SmemCtl& c, uint32_t qs, uint32_t qph, Tile& t,
+                                          volatile int* abort_flag, int* err) {
+  if (!warp_wait_bounded(smem_u32(&c.xfull[qs]), qph, abort_flag, err, TIMEOUT_NS)) return false;
+  lds_tile(smem_u32(&c.xq[qs]), t);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    mbar_expect_tx(smem_u32(&c.xfull[qs]), TILE_BYTES);
+    // the tile is in registers (the arrive takes a word of it as an operand), so a relaxed
+    // arrive cannot overtake the reads
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(mapa_shared(smem_u32(&c.xempty[qs]), 0)), "r"(t.prob) : "memory");
+  }
+  return true;
+}
+
+// Take slot `qs` of this CTA's local ring (one thread).
+__device__ __forceinline__ bool ring_take(SmemCtl& c, uint32_t qs, uint32_t qph, Tile& t,
+                                          volatile int* abort_flag, int* err) {
+  if (!mbar_wait_bounded(smem_u32(&c.lfull[qs]), qph, abort_flag, err, TIMEOUT_NS)) return false;
+  lds_tile(smem_u32(&c.lsq[qs]), t);
+  mbar_arrive(smem_u32(&c.lempty[qs]));
+  return true;
+}
+
+// Warp-wide ring_take: lane 0 waits, every lane reads the slot, lane 0 releases it.
+__device__ __forceinline__ bool ring_take_warp(SmemCtl& c, uint32_t qs, uint32_t qph, Tile& t,
+                                               volatile int* abort_flag, int* err) {
+  if (!warp_wait_bounded(smem_u32(&c.lfull[qs]), qph, abort_flag, err, TIMEOUT_NS)) return false;
+  lds_tile(smem_u32(&c.lsq[qs]), t);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&c.lempty[qs]));
+  return true;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -281,6 +405,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     for (int s = 0; s < STAGES; ++s) { mbar_init(bar(c.full[s]), 1); mbar_init(bar(c.empty[s]), 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(bar(c.tfull[a]), 1); mbar_init(bar(c.tempty[a]), 8); }
     mbar_init(bar(c.drain), 1);
+    for (int s = 0; s < SQ; ++s) {
+      mbar_init(bar(c.lfull[s]), 1);
+      mbar_init(bar(c.lempty[s]), rank == 0 ? LOCAL_READERS_0 : LOCAL_READERS_1);
+      mbar_init(bar(c.xfull[s]), 1);
+      mbar_init(bar(c.xempty[s]), 1);
+    }
+    mbar_init(bar(c.took), 1);
+    // the channel's first phases: one arrival (this one) and the tile's bytes
+    if (rank == 1)
+      for (int s = 0; s < SQ; ++s) mbar_expect_tx(bar(c.xfull[s]), TILE_BYTES);
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -290,9 +424,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   // finish together; then the tile prefix over that order (counts depend on device offsets)
   const int nprob = (MODE == MODE_GATE) ? 1 : p.n_routed + p.has_shared;
   for (int q = threadIdx.x; q < nprob; q += THREADS) {
-    int rows = p.T;
-    if (MODE != MODE_GATE && q < p.n_routed) rows = max(p.offsets[q + 1] - p.offsets[q], 0);
+    int rows = p.T, row0 = 0;
+    if (MODE != MODE_GATE && q < p.n_routed) {
+      row0 = p.offsets[q];
+      rows = max(p.offsets[q + 1] - row0, 0);
+    }
     c.rows[q] = rows;
+    c.row0[q] = row0;
   }
   __syncthreads();
   for (int q = threadIdx.x; q < nprob; q += THREADS) {
@@ -350,26 +488,42 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     }
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once / its parity
+    uint32_t qs = 0, qph = 0;                   // schedule ring slot and phase
     bool ok = true;
-    for (int tile = pair; tile < total && ok; tile += npairs) {
-      const Tile t = decode_tile<MODE>(p, c, tile);
+    while (ok) {
+      Tile t;
+      if (!ring_take_warp(c, qs, qph, t, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      if (++qs == SQ) { qs = 0; qph ^= 1u; }
+      if (t.prob < 0) break;
+      if (rank == 0 && lane == 0) mbar_arrive(bar(c.took));  // the scheduler may claim the next
       for (int kb = 0; kb < t.kb; ++kb) {
+        // everything the stage's copies need is computed before waiting for the slot
+        const int nu = min(UNITS, t.ku - kb * UNITS);             // units in this block
+        // lanes 0..7 serve unit 0, lanes 8..15 unit 1: lane 8u loads the weight box, lanes
+        // 8u + j (j < nbox) the token boxes
+        const int u = (lane >> 3) & 1, j = lane & 7;
+        const bool active = lane < 8 * nu;
+        const Boxes b = boxes_of<MODE>(p, t, t.ku0 + kb * UNITS + u, rank);
+        const uint32_t fb = mapa_shared(bar(c.full[stage]), 0);  // the first CTA's barrier
+        const uint32_t sa = sbase + stage * STAGE_BYTES + u * A_UNIT;
+        const uint32_t sb = sbase + stage * STAGE_BYTES + A_BYTES + u * B_UNIT + j * b.box_bytes;
+        const uint32_t tx = 2 * nu * (A_UNIT + t.nbox * b.box_bytes);
         if (!warp_wait_bounded(bar(c.empty[stage]), phase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
           ok = false;
           break;
         }
-        const uint32_t fb = mapa_shared(bar(c.full[stage]), 0);  // the first CTA's barrier
-        const uint32_t sa = sbase + stage * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-        const Boxes b = boxes_of<MODE>(p, t, t.kb0 + kb, rank);
-        if (lane == 0) {
-          if (rank == 0) mbar_expect_tx(bar(c.full[stage]), 2 * (A_BYTES + t.nbox * b.box_bytes));
-          if (MODE == MODE_UP) tma_load_5d_pair(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1);
-          else tma_load_2d_pair(sa, b.tw, fb, b.ax, b.ay0);
-        }
+        if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[stage]), tx);
         __syncwarp();
-        if (lane < t.nbox)
-          tma_load_2d_pair(sb + lane * b.box_bytes, b.tx, fb, b.bx, b.by0 + lane * b.box_rows);
+        if (active) {
+          if (j == 0) {
+            if (MODE == MODE_UP) tma_load_5d_pair(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1);
+            else tma_load_2d_pair(sa, b.tw, fb, b.ax, b.ay0);
+          }
+          if (j < t.nbox) tma_load_2d_pair(sb, b.tx, fb, b.bx, b.by0 + j * b.box_rows);
+        }
         __syncwarp();
         issued_mask |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -394,10 +548,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   } else if (warp == 1) {
     // ================================================================ MMA issuer (first CTA)
     if (rank == 0 && lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, aphase = 0, qs = 0, qph = 0;
       bool ok = true;
-      for (int tile = pair; tile < total && ok; tile += npairs) {
-        const Tile t = decode_tile<MODE>(p, c, tile);
+      while (ok) {
+        Tile t;
+        if (!ring_take(c, qs, qph, t, abort_flag, p.err)) break;
+        if (++qs == SQ) { qs = 0; qph ^= 1u; }
+        if (t.prob < 0) break;
         const uint32_t idesc = idesc_bf16_f32(2 * BM, t.ncols);
         if (!mbar_wait_bounded(bar(c.tempty[acc]), aphase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
           ok = false;
@@ -412,11 +569,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
           }
           tc_fence_after();
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint64_t ad = sdesc_k_sw128(sa);
-          const uint64_t bd = sdesc_k_sw128(sa + A_BYTES);
+          const int nu = min(UNITS, t.ku - kb * UNITS);
+          for (int u = 0; u < nu; ++u) {
+            const uint64_t ad = sdesc_k_sw128(sa + u * A_UNIT);
+            const uint64_t bd = sdesc_k_sw128(sa + A_BYTES + u * B_UNIT);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_f16_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < KU / 16; ++kk)
+              tc_mma_f16_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
+                              (kb > 0 || u > 0 || kk > 0) ? 1u : 0u);
+          }
           tc_commit_pair_mc(bar(c.empty[stage]), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -430,14 +591,47 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         grace_wait(bar(c.drain), 0);
       }
     }
+  } else if (warp == 6) {
+    // ================================================================ tile scheduler
+    // First CTA: tiles one per pair in pair order first; then either round robin (static) or,
+    // with a tile counter, in index order to whichever pair asks next: a pair claims its next
+    // tile when its producer starts the current one, so the pairs that share a weight tile start
+    // it within about a microsecond of each other and its second read hits L2. Each tile is
+    // decoded once here. Second CTA: relays the first CTA's tiles into its local ring.
+    uint32_t qs = 0, qph = 0, tph = 0;
+    int cur = pair;
+    for (;;) {
+      Tile t;
+      if (rank == 0) {
+        t = cur < total ? decode_tile<MODE>(p, c, cur) : end_tile();
+        if (!ring_publish(c, qs, qph, t, abort_flag, p.err) ||
+            !ring_send(c, qs, qph, t, abort_flag, p.err))
+          break;
+      } else {
+        if (!ring_recv(c, qs, qph, t, abort_flag, p.err) ||
+            !ring_publish(c, qs, qph, t, abort_flag, p.err))
+          break;
+      }
+      if (++qs == SQ) { qs = 0; qph ^= 1u; }
+      if (t.prob < 0) break;
+      if (rank == 0) {
+        if (!warp_wait_bounded(bar(c.took), tph, abort_flag, p.err, TIMEOUT_NS)) break;
+        tph ^= 1u;
+        if (lane == 0) cur = p.sched != nullptr ? npairs + atomicAdd(p.sched, 1) : cur + npairs;
+        cur = __shfl_sync(FULL_MASK, cur, 0);
+      }
+    }
   } else {
     // ================================================================ epilogue
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const uint32_t tempty0 = mapa_shared(bar(c.tempty[0]), 0);
     const uint32_t tempty1 = mapa_shared(bar(c.tempty[1]), 0);
-    uint32_t acc = 0, aphase = 0;
-    for (int tile = pair; tile < total; tile += npairs) {
-      const Tile t = decode_tile<MODE>(p, c, tile);
+    uint32_t acc = 0, aphase = 0, qs = 0, qph = 0;
+    for (;;) {
+      Tile t;
+      if (!ring_take_warp(c, qs, qph, t, abort_flag, p.err)) break;
+      if (++qs == SQ) { qs = 0; qph ^= 1u; }
+      if (t.prob < 0) break;
       if (!warp_wait_bounded(bar(c.tfull[acc]), aphase, abort_flag, p.err, TIMEOUT_NS)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
@@ -632,6 +826,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   prm.gate_bias = a.gate_bias;
   prm.splits = 1;
   prm.err = a.err;
+  prm.sched = a.mode == MODE_GATE ? nullptr : a.sched;
   const uint64_t H = a.H, I = a.I, S = a.S, N = a.N, T = a.T, R = a.rows_cap;
   bool ok = true;
   if (a.mode == MODE_GATE) {
@@ -640,7 +835,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
     // Few token tiles (decode): split the K range so that about every CTA pair has a tile;
     // the partial sums go to the caller's scratch and are reduced in a fixed order.
     const int tiles = (int)((T + TOK - 1) / TOK) * (int)((N + 2 * BM - 1) / (2 * BM));
-    const int kb_total = (int)(H / BK);
+    const int ku_total = (int)(H / KU);
+    const int kb_total = (ku_total + UNITS - 1) / UNITS;
     const int pairs = num_sms / 2;
     if (a.gate_part != nullptr && 2 * tiles <= pairs) {
       int want = pairs / tiles;
@@ -648,8 +844,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
       if ((size_t)want > fit) want = (int)fit;
       if (want > kb_total) want = kb_total;
       if (want > 1) {
-        prm.kb_per_split = (kb_total + want - 1) / want;
-        prm.splits = (kb_total + prm.kb_per_split - 1) / prm.kb_per_split;
+        const int kb_per_split = (kb_total + want - 1) / want;
+        prm.ku_per_split = kb_per_split * UNITS;
+        prm.splits = (kb_total + kb_per_split - 1) / kb_per_split;
         prm.gate_part = a.gate_part;
       }
     }

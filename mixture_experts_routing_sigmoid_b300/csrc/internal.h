@@ -125,6 +125,8 @@ struct GemmArgs {
   const float* gate_bias;   // MODE_GATE: [N] or nullptr
   float* gate_part;         // MODE_GATE split-K partial sums, or nullptr (no split)
   size_t gate_part_floats;  // capacity of gate_part
+  int* sched;               // UP / DOWN (tcgen05): tile counter, zero at launch, for the dynamic
+                            // tile schedule; nullptr: static round-robin schedule
   int* err;
 };
 // Rows (of N floats) of the gate GEMM's split-K scratch the workspace provides.

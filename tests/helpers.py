@@ -18,6 +18,12 @@ MID_B = CONFIGS["v1"].replace(
 MID_V2 = CONFIGS["v2"].replace(name="mid_v2", T=640, hidden=256, n_routed=40, n_groups=8,
                                topk_groups=3, top_k=6, n_shared=1, inter=128, w_std=0.05,
                                gate_std=0.06)
+# K = hidden = 320 is an odd multiple of 64: the router and up-projection GEMMs' last k block
+# holds one 64-element unit (and the router's split K range ends in it at small T)
+MID_ODD = CONFIGS["v3_prefill"].replace(
+    name="mid_odd", T=333, hidden=320, n_routed=24, n_groups=4, topk_groups=2, top_k=4,
+    group_score_topn=2, n_shared=2, inter=256, w_std=0.05, gate_std=0.06,
+    logit_offset="zipf")
 
 
 def rel_frob(a, b) -> float:

@@ -10,11 +10,11 @@ import torch
 
 import oracle
 from moe_inputs import CONFIGS, make_logits, make_router, make_weights, make_x
-from tests.helpers import MID_A, MID_B, MID_V2, rel_frob, sample_tokens, tol_for, workspace
+from tests.helpers import MID_A, MID_B, MID_ODD, MID_V2, rel_frob, sample_tokens, tol_for, workspace
 
 pytestmark = pytest.mark.gpu
 
-CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2}
+CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_odd": MID_ODD}
 
 
 def _perm_inputs(cfg, seed=3):
@@ -32,7 +32,7 @@ def _expert_of_rows(offs):
     return np.repeat(np.arange(len(offs) - 1), np.diff(offs))
 
 
-@pytest.mark.parametrize("name", ["tiny", "mid_a", "mid_b", "mid_v2", "v1", "v2",
+@pytest.mark.parametrize("name", ["tiny", "mid_a", "mid_b", "mid_v2", "mid_odd", "v1", "v2",
                                   "v3_prefill", "v3_decode_32", "v3_decode_512"])
 def test_expert_ffn(name):
     import mixture_experts_routing_sigmoid_b300 as moe

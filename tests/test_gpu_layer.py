@@ -12,11 +12,11 @@ import torch
 
 import oracle
 from moe_inputs import CONFIGS, make_weights, make_x
-from tests.helpers import MID_A, MID_B, MID_V2, rel_frob, sample_tokens, tol_for, workspace
+from tests.helpers import MID_A, MID_B, MID_ODD, MID_V2, rel_frob, sample_tokens, tol_for, workspace
 
 pytestmark = pytest.mark.gpu
 
-CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2}
+CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_odd": MID_ODD}
 
 
 def _near_cut_tokens(cfg, idx, w, kept, band=3):
@@ -87,7 +87,7 @@ class _RowFetcher:
 
 
 @pytest.mark.parametrize("name,n_sample", [("tiny", 64), ("mid_a", 300), ("mid_b", 517),
-                                           ("mid_v2", 640)])
+                                           ("mid_v2", 640), ("mid_odd", 333)])
 def test_layer_small_whole(name, n_sample):
     _run(CFGS[name], n_sample)
 

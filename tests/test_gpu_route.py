@@ -11,11 +11,11 @@ import torch
 
 import oracle
 from moe_inputs import CONFIGS, make_logits, make_router, make_x
-from tests.helpers import MID_A, MID_B, MID_V2, gpu_route, sample_tokens, workspace
+from tests.helpers import MID_A, MID_B, MID_ODD, MID_V2, gpu_route, sample_tokens, workspace
 
 pytestmark = pytest.mark.gpu
 
-ROUTE_CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2,
+ROUTE_CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_odd": MID_ODD,
               "k16": CONFIGS["v1"].replace(name="k16", T=1000, n_routed=64, n_groups=4,
                                            topk_groups=4, top_k=16, group_score_topn=2,
                                            score_fn="sigmoid", norm_topk=True,
