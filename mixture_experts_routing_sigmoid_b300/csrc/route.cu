@@ -56,21 +56,18 @@ struct Selection {
   double emargin;  // K-th key minus best remaining eligible key (+inf if none)
   double gkth;     // Gk-th group score
   double gmargin;  // Gk-th minus (Gk+1)-th group score (+inf if G == Gk)
+  uint32_t gmask;  // chosen groups
   bool ok;
 };
 
-// Group-limited top-K over keys held lane-strided (expert e = j*32 + lane).
+// Group scores (sum of each group's top-n keys, n = 1 or 2) of keys held lane-strided (expert
+// e = j*32 + lane): lane g < G returns group g's score, the other lanes -inf.
 template <typename KT>
-__device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int lane, int N, int K,
-                                                    int G, int Gk, int topn, int J) {
-  Selection out;
-  out.ok = true;
+__device__ __forceinline__ KT group_scores(const KT (&key)[MAXJ], int lane, int N, int G, int topn,
+                                           int J) {
   const int gsz = N / G;
-  uint32_t gmask = 0xffffffffu;
-  out.gmargin = INFINITY;
-  out.gkth = INFINITY;
-  if (G > 1) {
-    KT my_gs = neg_inf<KT>();
+  KT my_gs = neg_inf<KT>();
+  {
     if (gsz == 32 && G == J) {
       // group g is register g of every lane: reduce all groups' top-2 side by side
       KT a1[MAXJ], a2[MAXJ];
@@ -116,6 +113,22 @@ __device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int l
         if (lane == g) my_gs = gsv;
       }
     }
+  }
+  return my_gs;
+}
+
+// Group-limited top-K over keys held lane-strided (expert e = j*32 + lane).
+template <typename KT>
+__device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int lane, int N, int K,
+                                                    int G, int Gk, int topn, int J) {
+  Selection out;
+  out.ok = true;
+  const int gsz = N / G;
+  uint32_t gmask = 0xffffffffu;
+  out.gmargin = INFINITY;
+  out.gkth = INFINITY;
+  if (G > 1) {
+    const KT my_gs = group_scores<KT>(key, lane, N, G, topn, J);
     gmask = 0;
     bool taken = false;
     KT last = neg_inf<KT>();
@@ -134,6 +147,7 @@ __device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int l
     }
     out.gkth = (double)last;
   }
+  out.gmask = gmask;
 
   uint32_t elig = 0, taken = 0;
 #pragma unroll
@@ -173,6 +187,201 @@ __device__ __forceinline__ float key_tol(double v) {
   // (expf <= 2 ulp, one IEEE division, one sum), the + bias one rounding; 2e-6 * max(1,|v|)
   // is several times that bound.
   return 2e-6f * fmaxf(1.0f, fabsf((float)v));
+}
+
+// One out-of-line copy: the recheck runs for a handful of tokens per launch, with its code
+// fetched cold, so its size (not its arithmetic) sets its cost.
+__device__ __noinline__ double exact_sigmoid_key(float u, float b) {
+  return 1.0 / (1.0 + exp(-(double)u)) + (double)b;
+}
+
+// Order-preserving map of a (non-NaN) double onto a signed 64-bit integer: comparisons of the
+// exact keys run on the integer pipes instead of the (slow) fp64 one.
+__device__ __forceinline__ long long ord64(double d) {
+  const long long i = __double_as_longlong(d);
+  return i >= 0 ? i : i ^ 0x7fffffffffffffffll;
+}
+constexpr long long ORD_NONE = (long long)0x8000000000000000ull;  // below every ord64
+__device__ __forceinline__ double unord64(long long o) {
+  return __longlong_as_double(o >= 0 ? o : o ^ 0x7fffffffffffffffll);
+}
+
+// Warp-wide argmax on (ordered key desc, index asc); result in every lane.
+__device__ __forceinline__ void warp_argmax_ord(long long& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long ov = __shfl_xor_sync(FULL_MASK, v, o);
+    const int oi = __shfl_xor_sync(FULL_MASK, i, o);
+    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+  }
+}
+
+// Exact selection for a sigmoid gate whose fp32 decision lies within its error bound. Every
+// fp32 key is within tol of its exact (fp64) value and every fp32 group score within gtol, so a
+// group whose fp32 score exceeds the Gk-th by more than 2 gtol is among the exact best Gk, one
+// below it by more than 2 gtol is not, and only the groups inside that band are rescored in
+// fp64 (all their experts) when the band holds more groups than places left; likewise for the
+// experts around the K-th eligible key with 2 tol. The band's members are ranked by their exact
+// values (ties: lower index). The keys are recomputed here from the logits exactly as the fp32
+// pass computes them. Lane r < K receives the r-th chosen expert in ascending order; false if a
+// rank is missing (the caller then redoes the token entirely in fp64). fp_gmask and fp_kth are
+// the fp32 pass's chosen groups and K-th key: when the groups stand, its K-th key is reused.
+__device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, int lane, int N,
+                                            int K, int G, int Gk, int topn, uint32_t fp_gmask,
+                                            float fp_kth, int& sel_e) {
+  constexpr int NONE = 0x7fffffff;
+  const int J = (N + 31) >> 5;
+  const int gsz = N / G;
+  float u[MAXJ], b[MAXJ], key[MAXJ];
+  float kmax = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < MAXJ; ++j) {
+    const int e = j * 32 + lane;
+    const bool v = j < J && e < N;
+    u[j] = v ? ut[e] : -INFINITY;
+    b[j] = (v && bias != nullptr) ? bias[e] : 0.0f;
+    const float s = 1.0f / (1.0f + expf(-u[j]));
+    key[j] = v ? s + b[j] : -INFINITY;
+    if (v) kmax = fmaxf(kmax, fabsf(key[j]));
+  }
+  kmax = warp_max(kmax);
+
+  uint32_t gmask = 0xffffffffu;
+  if (G > Gk) {
+    const float gs = group_scores<float>(key, lane, N, G, topn, J);
+    int rnk = 0;  // rank of this lane's group (ties: lower group)
+    for (int g = 0; g < G; ++g) {
+      const float v = __shfl_sync(FULL_MASK, gs, g);
+      if (lane < G && (v > gs || (v == gs && g < lane))) ++rnk;
+    }
+    const uint32_t at = __ballot_sync(FULL_MASK, lane < G && rnk == Gk - 1);
+    const double vg = (double)__shfl_sync(FULL_MASK, gs, __ffs(at) - 1);
+    const double gtol = topn * (double)key_tol(kmax) + 6e-8 * fabs(vg);
+    const bool in = lane < G && (double)gs > vg + 2.0 * gtol;
+    const uint32_t cin = __ballot_sync(FULL_MASK, in);
+    const uint32_t band = __ballot_sync(FULL_MASK, lane < G && !in && (double)gs >= vg - 2.0 * gtol);
+    const int need = Gk - __popc(cin);
+    uint32_t picked = 0;
+    if (__popc(band) == need) {
+      picked = band;  // every band group is in: no exact score needed
+    } else {
+      long long gx = ORD_NONE;  // lane g: exact score of band group g (ordered)
+      for (uint32_t m = band; m; m &= m - 1) {
+        const int g = __ffs(m) - 1;
+        long long a1 = ORD_NONE, a2 = ORD_NONE;
+        if (gsz == 32 && G == J) {  // group g is register g of every lane
+          a1 = ord64(exact_sigmoid_key(u[g], b[g]));
+        } else {
+#pragma unroll 1
+          for (int j = 0; j < MAXJ; ++j) {
+            const int e = j * 32 + lane;
+            const bool mine = j < J && e < N && e / gsz == g;
+            if (__any_sync(FULL_MASK, mine) && mine) {
+              const long long o = ord64(exact_sigmoid_key(u[j], b[j]));
+              if (o > a1) { a2 = a1; a1 = o; } else if (o > a2) { a2 = o; }
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {  // top-2 of the group, compared as integers
+          const long long b1 = __shfl_xor_sync(FULL_MASK, a1, o);
+          const long long b2 = __shfl_xor_sync(FULL_MASK, a2, o);
+          if (b1 > a1) { a2 = max(a1, b2); a1 = b1; }
+          else { a2 = max(a2, b1); }
+        }
+        if (lane == g) gx = ord64(topn == 1 ? unord64(a1) : unord64(a1) + unord64(a2));
+      }
+      for (int r = 0; r < need; ++r) {
+        const bool cand = ((band & ~picked) >> lane) & 1u;
+        long long v = cand ? gx : ORD_NONE;
+        int i = cand ? lane : NONE;
+        warp_argmax_ord(v, i);
+        if (i == NONE) return false;
+        picked |= 1u << i;
+      }
+    }
+    gmask = cin | picked;
+  }
+
+  uint32_t elig = 0;
+#pragma unroll 1
+  for (int j = 0; j < MAXJ; ++j) {
+    const int e = j * 32 + lane;
+    if (j < J && e < N && ((gmask >> (e / gsz)) & 1u)) elig |= 1u << j;
+  }
+  float vk = fp_kth;  // K-th best fp32 eligible key
+  uint32_t taken = 0;
+  for (int r = 0; r < K && gmask != fp_gmask; ++r) {
+    float v = -INFINITY;
+    int i = NONE;
+#pragma unroll 1
+    for (int j = 0; j < MAXJ; ++j)
+      if (((elig & ~taken) >> j) & 1u)
+        if (key[j] > v || i == NONE) { v = key[j]; i = j * 32 + lane; }
+    warp_argmax(v, i);
+    if (i == NONE) return false;
+#pragma unroll 1
+    for (int j = 0; j < MAXJ; ++j)
+      if (i == j * 32 + lane) taken |= 1u << j;
+    vk = v;
+  }
+  const double tol = 2.0 * (double)key_tol(vk);
+  uint32_t cin = 0, band = 0;
+#pragma unroll 1
+  for (int j = 0; j < MAXJ; ++j) {
+    if ((elig >> j) & 1u) {
+      const double d = (double)key[j] - (double)vk;
+      if (d > tol) cin |= 1u << j;
+      else if (d >= -tol) band |= 1u << j;
+    }
+  }
+  const int need = K - warp_sum(__popc(cin));
+  uint32_t picked = 0;
+  if (warp_sum(__popc(band)) == need) {
+    picked = band;  // every band expert is in
+  } else {
+    long long kd[MAXJ];
+#pragma unroll 1
+    for (int j = 0; j < MAXJ; ++j) {
+      kd[j] = ORD_NONE;
+      const bool mine = (band >> j) & 1u;
+      if (__any_sync(FULL_MASK, mine) && mine) kd[j] = ord64(exact_sigmoid_key(u[j], b[j]));
+    }
+    for (int r = 0; r < need; ++r) {
+      long long v = ORD_NONE;
+      int i = NONE;
+#pragma unroll 1
+      for (int j = 0; j < MAXJ; ++j)
+        if (((band & ~picked) >> j) & 1u)
+          if (kd[j] > v || i == NONE) { v = kd[j]; i = j * 32 + lane; }
+      warp_argmax_ord(v, i);
+      if (i == NONE) return false;
+#pragma unroll 1
+      for (int j = 0; j < MAXJ; ++j)
+        if (i == j * 32 + lane) picked |= 1u << j;
+    }
+  }
+  // lane r < K takes the r-th chosen expert (any order: the caller sorts them)
+  __shared__ int slot[256 / 32][32];
+  const uint32_t chosen = cin | picked;
+  const int cnt = __popc(chosen);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int total = __shfl_sync(FULL_MASK, incl, 31);
+  if (total != K) return false;
+  int* sw = slot[threadIdx.x >> 5];
+  int pos = incl - cnt;
+#pragma unroll 1
+  for (int j = 0; j < MAXJ; ++j)
+    if ((chosen >> j) & 1u) sw[pos++] = j * 32 + lane;
+  __syncwarp();
+  sel_e = lane < K ? sw[lane] : -1;
+  __syncwarp();
+  return true;
 }
 
 __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
@@ -241,11 +450,20 @@ __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
              (a.G > a.Gk && sel.gmargin <= 2.0 * gtol);
     }
     redo = __any_sync(FULL_MASK, redo);
+    int sel_e = sel.e;
+    if (redo && sigmoid && sel.ok && !a.precise_w) {
+      // rescore only the groups and experts within the error bound of a decision
+      int e_ref = -1;
+      if (refine_sigmoid(ut, a.bias, lane, a.N, a.K, a.G, a.Gk, a.topn, sel.gmask, (float)sel.kth,
+                         e_ref)) {
+        sel_e = e_ref;
+        redo = false;
+      }
+    }
 
     // ---- weights: scores of the chosen experts (fp32 unless an fp64 pass is needed)
     double sd_z = 0.0;  // fp64 softmax normaliser (fp64 passes only)
     double sel_s = 0.0;
-    int sel_e = sel.e;
     const bool need_f64 = redo || a.precise_w;
     if (need_f64) {
       double sd[MAXJ];
