@@ -153,10 +153,10 @@ def layer_work(cfg, counts, kept_rows: int) -> dict:
                 weight_bytes=(touched + S) * 3.0 * H * I * eb)
 
 
-def traffic_per_launch(up_flops: float):
-    """DRAM bytes per launch of the up GEMM from the committed ncu capture, scaled from the
-    profiled case by algorithmic FLOPs (weights and token rows both grow with the work), or
-    None when the kernel source has changed since the counters were taken."""
+def traffic_per_launch(workload: str):
+    """DRAM bytes (read + write) of one launch of the up GEMM on this workload, from the committed
+    ncu capture of that workload; None when there is no capture of it or the kernel source has
+    changed since the counters were taken."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     src = os.path.join(ROOT, "mixture_experts_routing_sigmoid_b300", "csrc", "gemm_tc.cu")
@@ -165,7 +165,8 @@ def traffic_per_launch(up_flops: float):
     d = json.load(open(p)).get("tc_gemm_kernel<MODE_UP>")
     if not d or d.get("source_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
         return None
-    return d["dram_bytes_per_launch"] / d["algorithmic_flops_per_launch"] * up_flops
+    c = d.get("captures", {}).get(workload)
+    return None if c is None else float(c["dram_read_bytes"] + c["dram_write_bytes"])
 
 
 def workload_name(cfg) -> str:
@@ -296,7 +297,7 @@ def run_ours(args, world, rank, local):
     if stages and ncalls:
         per = {k: v / ncalls for k, v in stages.items()}
         up = per["up"]
-        traffic = traffic_per_launch(work["up_flops"])
+        traffic = traffic_per_launch(cfg.name)
         if result["layer_roofline"]["bound"] == "tensor":
             up_tf = work["up_flops"] / (up * 1e-3) / 1e12
             result["roofline"] = {
