@@ -154,12 +154,15 @@ __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
   }
 }
 
-// Batches of at most one block (T <= 256): histogram, scan and scatter in one CTA, the same
-// arithmetic as the three kernels above with the per-block state kept in shared memory.
-__global__ void __launch_bounds__(PB) perm_single_block_kernel(PermuteArgs p) {
-  extern __shared__ uint32_t sm[];  // [N][8] masks, then [N + 1] exclusive offsets
-  int* excl = reinterpret_cast<int*>(sm + p.N * 8);
-  for (int i = threadIdx.x; i < p.N * 8; i += PB) sm[i] = 0;
+// Batches of at most SB_MAX_T tokens: histogram, scan and scatter in one CTA (one thread per
+// token, at least one per expert), the same arithmetic as the three kernels above with the
+// bitmasks ([N][W] words, W = ceil(T / 32)) in shared memory.
+constexpr int SB_MAX_T = 1024;
+__global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs p) {
+  extern __shared__ uint32_t sm[];  // [N][W] masks, then [N + 1] exclusive offsets
+  const int W = (p.T + 31) >> 5;
+  int* excl = reinterpret_cast<int*>(sm + p.N * W);
+  for (int i = threadIdx.x; i < p.N * W; i += blockDim.x) sm[i] = 0;
   __syncthreads();
   const int t = threadIdx.x;
   if (t < p.T) {
@@ -167,19 +170,17 @@ __global__ void __launch_bounds__(PB) perm_single_block_kernel(PermuteArgs p) {
       const long long a = (long long)t * p.K + k;
       const int e = p.idx[a];
       if (e < 0 || e >= p.N) { set_error(p.err, ERR_DEVICE_CHECK); continue; }
-      if (is_kept(p, a, e)) atomicOr(&sm[e * 8 + (t >> 5)], 1u << (t & 31));
+      if (is_kept(p, a, e)) atomicOr(&sm[e * W + (t >> 5)], 1u << (t & 31));
     }
   }
   __syncthreads();
   {
-    // exclusive scan of the per-expert counts (N <= 256 = PB): warp scans, then warp totals
-    __shared__ int wsum[PB / 32];
+    // exclusive scan of the per-expert counts (N <= blockDim): warp scans, then warp totals
+    __shared__ int wsum[SB_MAX_T / 32];
     const int e = threadIdx.x, lane = e & 31, wi = e >> 5;
     int cnt = 0;
-    if (e < p.N) {
-#pragma unroll
-      for (int w = 0; w < 8; ++w) cnt += __popc(sm[e * 8 + w]);
-    }
+    if (e < p.N)
+      for (int w = 0; w < W; ++w) cnt += __popc(sm[e * W + w]);
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(PB) perm_single_block_kernel(PermuteArgs p) {
       const long long a = (long long)t * p.K + k;
       const int e = p.idx[a];
       if (e < 0 || e >= p.N || !is_kept(p, a, e)) { p.slot_row[a] = -1; continue; }
-      const uint32_t* m = sm + e * 8;
+      const uint32_t* m = sm + e * W;
       int rank = __popc(m[wi] & below);
       for (int i = 0; i < wi; ++i) rank += __popc(m[i]);
       const int row = excl[e] + rank;
@@ -253,8 +254,11 @@ cudaError_t launch_permute(const PermuteArgs& p, int num_sms, cudaStream_t st) {
     drop_threshold_kernel<<<p.D, 1024, 0, st>>>(p);
     note_launches(1);
   }
-  if (nb == 1) {
-    perm_single_block_kernel<<<1, PB, (p.N * 8 + p.N + 1) * sizeof(uint32_t), st>>>(p);
+  if (p.T <= SB_MAX_T) {
+    const int W = (p.T + 31) / 32;
+    int threads = ((p.T + 31) / 32) * 32;
+    if (threads < p.N) threads = ((p.N + 31) / 32) * 32;
+    perm_single_block_kernel<<<1, threads, (p.N * W + p.N + 1) * sizeof(uint32_t), st>>>(p);
     note_launches(1);
     return cudaGetLastError();
   }

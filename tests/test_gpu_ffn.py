@@ -117,3 +117,34 @@ def test_combine(name):
     if cfg.dtype == "bf16":
         # output is the bf16 rounding of an fp32 sum: elementwise within 2^-8 relative + slack
         assert np.all(np.abs(got - want) <= 2 ** -8 * np.abs(want) + 1e-2)
+
+
+@pytest.mark.parametrize("name", ["mid_a", "v3_prefill_e32"])
+def test_tile_schedule_does_not_change_results(name):
+    """moe_expert_ffn (workspace given: tiles claimed dynamically from a counter) and
+    moe_expert_up + moe_expert_down (no workspace: static round-robin tiles) compute every output
+    tile with the same k order, so their outputs are bitwise equal."""
+    import mixture_experts_routing_sigmoid_b300 as moe
+    cfg = CFGS[name]
+    T, H, K, I, S = cfg.T, cfg.hidden, cfg.top_k, cfg.inter, cfg.n_shared
+    dev = "cuda"
+    w = make_weights(cfg, device=dev)
+    x = make_x(cfg, device=dev, seed=2)
+    idx, wt, offs, row_token, slot_row = _perm_inputs(cfg)
+    R = int(offs[-1])
+    x_perm = torch.zeros((T * K, H), dtype=x.dtype, device=dev)
+    x_perm[:R] = x[torch.from_numpy(row_token).long().to(dev)]
+    offs_d = torch.from_numpy(offs).to(dev)
+    y_dyn = torch.zeros((T * K, H), dtype=x.dtype, device=dev)
+    ys_dyn = torch.zeros((T, H), dtype=x.dtype, device=dev)
+    moe.moe_expert_ffn(cfg, T, x_perm, offs_d, x, w, y_dyn, ys_dyn, workspace(cfg, T))
+    h = torch.zeros((T * K, I), dtype=x.dtype, device=dev)
+    h_sh = torch.zeros((T, S * I), dtype=x.dtype, device=dev)
+    y_st = torch.zeros_like(y_dyn)
+    ys_st = torch.zeros_like(ys_dyn)
+    moe.moe_expert_up(cfg, T, x_perm, offs_d, x, w, h, h_sh)
+    moe.moe_expert_down(cfg, T, h, offs_d, h_sh, w, y_st, ys_st)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error() == 0
+    assert torch.equal(y_dyn[:R], y_st[:R])
+    assert torch.equal(ys_dyn, ys_st)

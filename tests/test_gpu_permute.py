@@ -92,3 +92,12 @@ def test_permute_end_to_end_from_gpu_route():
     np.testing.assert_array_equal(offs.cpu().numpy(), offs_o)
     np.testing.assert_array_equal(sr.cpu().numpy(), sr_o.ravel())
     np.testing.assert_array_equal(rt.cpu().numpy()[:offs_o[-1]], rt_o)
+
+
+@pytest.mark.parametrize("T", [1, 255, 257, 1023, 1024, 1025])
+def test_permute_single_block_boundaries(T):
+    """One CTA takes batches of up to 1024 tokens, more go through the three-kernel path: both
+    sides of the boundary are bit-exact."""
+    cfg = MID_A.replace(T=T)
+    idx, w = _oracle_routing(cfg, T)
+    _check(cfg, T, idx, w, with_x=True)

@@ -136,3 +136,24 @@ def test_route_end_to_end_from_x(name):
     assert n_ex <= max(3, len(tok) // 20)
     np.testing.assert_array_equal(idx_g.cpu().numpy()[tok][keep], idx_o[keep])
     assert np.abs(w_g.cpu().numpy()[tok][keep] - w_o[keep]).max() <= 1e-4
+
+
+@pytest.mark.parametrize("name", ["v3_prefill", "mid_a", "k16"])
+def test_route_dense_near_ties_sigmoid(name):
+    """Every token's keys sit within a few ulps of each other (one logit per token moved by 0-3
+    ulps per expert, a selection bias of 0.1 moved by 0-5 ulps per expert), so every group and
+    expert decision lies inside the fp32 error bound and is settled by the exact recheck, with
+    bands that hold most groups and experts and exact ties among them."""
+    cfg = ROUTE_CFGS[name]
+    N, T = cfg.n_routed, 256
+    rng = np.random.default_rng(21)
+    u0 = rng.standard_normal(T).astype(np.float32)
+    steps = rng.integers(0, 4, size=(T, N))
+    u = u0[:, None].repeat(N, axis=1)
+    for k in range(1, 4):
+        u = np.where(steps >= k, np.nextafter(u, np.float32(np.inf)), u)
+    b = np.full(N, 0.1, dtype=np.float32)
+    bsteps = rng.integers(0, 6, size=N)
+    for k in range(1, 6):
+        b = np.where(bsteps >= k, np.nextafter(b, np.float32(np.inf)), b)
+    _check_route(cfg, torch.from_numpy(u.astype(np.float32)), torch.from_numpy(b), name + " dense ties")
