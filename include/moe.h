@@ -19,6 +19,8 @@
  *   - Every tensor pointer is a DEVICE pointer on the current CUDA device unless stated, owned
  *     by the caller. The library allocates no device memory: scratch comes from `ws`, whose
  *     size moe_workspace_size() gives (one size fits every call for a given config and T).
+ *     A workspace serves one call at a time: two calls in flight on different streams need
+ *     two workspaces (it holds intermediates and the expert GEMMs' tile counters).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *     Nothing synchronises except moe_get_error().
  *   - Argument errors are returned synchronously before anything is launched; the text of the
@@ -175,13 +177,16 @@ moe_status moe_permute_static_scratch(const moe_config* cfg, int32_t T, const in
  *   x_perm [T*K, H], offsets [N+1] (device; rows per expert are read on the device),
  *   x [T, H] (shared experts; may be NULL iff S == 0), y_perm [T*K, H] out, y_shared [T, H] out
  *   (NULL iff S == 0). h is rounded to dtype between the two GEMMs.
+ *   ws holds h and the tile counters that let CTA pairs claim GEMM tiles as they free up (the
+ *   outputs do not depend on which pair computes a tile).
  */
 moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const void* x_perm,
                           const int32_t* offsets, const void* x, const moe_weights* w,
                           void* y_perm, void* y_shared, void* ws, size_t ws_bytes,
                           moe_stream_t stream);
 
-/* The two halves of moe_expert_ffn, exposed so each GEMM can be timed on its own.
+/* The two halves of moe_expert_ffn, exposed so each GEMM can be timed on its own. With no
+ * workspace they hand out tiles round robin; outputs are bitwise equal to moe_expert_ffn's.
  *   h [T*K, I] dtype out/in;  h_shared [T, S*I] dtype out/in (NULL iff S == 0). */
 moe_status moe_expert_up(const moe_config* cfg, int32_t T, const void* x_perm,
                          const int32_t* offsets, const void* x, const moe_weights* w, void* h,
