@@ -64,6 +64,11 @@ def max_over_ranks(v: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def job_tokens_per_s(ms_max: float, world: int, tokens_per_step: int, steps: int) -> float:
+    """Whole-job throughput: the tokens every replica processed over the slowest replica's time."""
+    return world * tokens_per_step * steps / (ms_max / 1e3)
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -247,7 +252,7 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device error {st} in the timed region")
     ms_max = max_over_ranks(ms, world, dev)
     ms_step = ms_max / args.steps
-    tok_s = world * T * args.steps / (ms_max / 1e3)
+    tok_s = job_tokens_per_s(ms_max, world, T, args.steps)
 
     # routing outcome of this batch (for the work accounting)
     idx = torch.empty((T, K), dtype=torch.int32, device=dev)
@@ -380,7 +385,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         del graph
         e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-        result["e2e"] = {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        result["e2e"] = {"value": job_tokens_per_s(e2e_ms, world, T, args.steps), "unit": "tokens/s",
                          "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                          "d2h_bytes_per_step": oh[0].numel() * oh[0].element_size(),
                          "overlap": "inputs and outputs double-buffered on two copy streams"}
