@@ -143,12 +143,13 @@ moe_status moe_load_stats(const moe_config* cfg, int32_t T, const float* logits,
  * segment in ascending token order.
  *   topk_idx, topk_w [T, K] from moe_route;  x [T, H] dtype or NULL (then x_perm is not written)
  *   offsets [N+1] int32 out (offsets[N] = rows kept R);  row_token [T*K] int32 out (first R used)
+ *   row_w [T*K] fp32 out or NULL: row_w[r] = topk_w of the assignment placed at row r (r < R)
  *   slot_row [T*K] int32 out: row of assignment (t,k), -1 if dropped;
  *   x_perm [T*K, H] dtype out: x_perm[r] = x[row_token[r]] for r < R.
  */
 moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
                        const float* topk_w, const void* x, int32_t* offsets, int32_t* row_token,
-                       int32_t* slot_row, void* x_perm, void* ws, size_t ws_bytes,
+                       float* row_w, int32_t* slot_row, void* x_perm, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
 /*

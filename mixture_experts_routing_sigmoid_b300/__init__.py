@@ -80,7 +80,7 @@ def _load():
         "moe_workspace_size": (SZ, [CFG, I32]),
         "moe_route": (I32, [CFG, I32, P, W, P, P, P, P, P, SZ, P]),
         "moe_load_stats": (I32, [CFG, I32, P, P, P, P, P, P, P, SZ, P]),
-        "moe_permute": (I32, [CFG, I32, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_permute": (I32, [CFG, I32, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_permute_static_scratch": (I32, [CFG, I32, P, P, P, P, P, P, P, P]),
         "moe_expert_ffn": (I32, [CFG, I32, P, P, P, W, P, P, P, SZ, P]),
         "moe_expert_up": (I32, [CFG, I32, P, P, P, W, P, P, P]),
@@ -192,10 +192,11 @@ def moe_load_stats(cfg, T, logits, topk_idx, counts, f, P, lb_z, ws, stream=None
 
 
 def moe_permute(cfg, T, topk_idx, topk_w, x, offsets, row_token, slot_row, x_perm, ws,
-                stream=None):
+                stream=None, row_w=None):
+    """row_w (optional, [T*K] fp32) is a keyword here; the C call takes it after row_token."""
     p, n = _ws(ws)
     _check(lib.moe_permute(ctypes.byref(_cfg(cfg)), int(T), _ptr(topk_idx), _ptr(topk_w),
-                           _ptr(x), _ptr(offsets), _ptr(row_token), _ptr(slot_row),
+                           _ptr(x), _ptr(offsets), _ptr(row_token), _ptr(row_w), _ptr(slot_row),
                            _ptr(x_perm), p, n, _stream(stream)), "moe_permute")
 
 

@@ -257,14 +257,16 @@ moe_status do_stats(const moe_config* c, int32_t T, const float* u, const int32_
 }
 
 moe_status do_permute(const moe_config* c, int32_t T, const int32_t* idx, const float* wt,
-                      const void* x, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
+                      const void* x, int32_t* offsets, int32_t* row_token, float* row_w,
+                      int32_t* slot_row,
                       void* x_perm, void* ws, cudaStream_t st) {
   const Layout L = layout(c, T);
   PermuteArgs p;
   p.T = T; p.N = c->n_routed; p.K = c->top_k; p.D = c->n_groups;
   p.capacity_drop = c->capacity_drop ? 1 : 0;
   p.idx = idx; p.w = wt; p.x = x; p.H = c->hidden; p.elem_bytes = c->dtype == MOE_BF16 ? 2 : 4;
-  p.offsets = offsets; p.row_token = row_token; p.slot_row = slot_row; p.x_perm = x_perm;
+  p.offsets = offsets; p.row_token = row_token; p.row_w = row_w; p.slot_row = slot_row;
+  p.x_perm = x_perm;
   p.masks = at<uint32_t>(ws, L.masks);
   p.cnt = at<int32_t>(ws, L.cnt);
   p.base = at<int32_t>(ws, L.base);
@@ -369,7 +371,7 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
   if (counts != nullptr || lb_z != nullptr)
     TRY(do_stats(cfg, T, u, idx, counts, nullptr, nullptr, lb_z, ws, st));
   stage_mark(STAGE_PERMUTE, st);
-  TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, slot_row, xy, ws, st));
+  TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, nullptr, slot_row, xy, ws, st));
   int32_t* sched = at<int32_t>(ws, L.sched);
   stage_mark(STAGE_UP, st);
   TRY(reset_sched(cfg, T, ws, st));
@@ -453,6 +455,7 @@ moe_status moe_load_stats(const moe_config* cfg, int32_t T, const float* logits,
 
 moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
                        const float* topk_w, const void* x, int32_t* offsets, int32_t* row_token,
+                       float* row_w,
                        int32_t* slot_row, void* x_perm, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
   g_detail[0] = 0;
@@ -464,10 +467,11 @@ moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_idx
     CHECK_PTR(row_token);
     CHECK_PTR(slot_row);
     CHECK_ALIGN(x);
+    CHECK_ALIGN(row_w);
     if (x != nullptr) CHECK_PTR(x_perm);
   }
   TRY(check_ws(cfg, T, ws, ws_bytes));
-  return do_permute(cfg, T, topk_idx, topk_w, x, offsets, row_token, slot_row, x_perm, ws,
+  return do_permute(cfg, T, topk_idx, topk_w, x, offsets, row_token, row_w, slot_row, x_perm, ws,
                     S_(stream));
 }
 

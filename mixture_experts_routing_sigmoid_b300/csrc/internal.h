@@ -79,6 +79,7 @@ struct PermuteArgs {
   int H, elem_bytes;
   int32_t* offsets;     // [N+1]
   int32_t* row_token;   // [T*K]
+  float* row_w;         // [T*K] or nullptr: routing weight of the assignment at each row
   int32_t* slot_row;    // [T*K]
   void* x_perm;         // [T*K, H]
   // scratch

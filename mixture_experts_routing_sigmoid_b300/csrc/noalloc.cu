@@ -103,7 +103,8 @@ extern "C" moe_status moe_permute_static_scratch(const moe_config* cfg, int32_t 
   p.capacity_drop = cfg->capacity_drop ? 1 : 0;
   p.idx = topk_idx; p.w = topk_w; p.x = x; p.H = cfg->hidden;
   p.elem_bytes = cfg->dtype == MOE_BF16 ? 2 : 4;
-  p.offsets = offsets; p.row_token = row_token; p.slot_row = slot_row; p.x_perm = x_perm;
+  p.offsets = offsets; p.row_token = row_token; p.row_w = nullptr; p.slot_row = slot_row;
+  p.x_perm = x_perm;
   p.masks = reinterpret_cast<uint32_t*>(base);
   p.cnt = reinterpret_cast<int32_t*>(base + kMaskBytes);
   p.base = reinterpret_cast<int32_t*>(base + kMaskBytes + kCountBytes);

@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
     const int row = p.base[(size_t)blockIdx.x * p.N + e] + rank;
     p.slot_row[a] = row;
     p.row_token[row] = t;
+    if (p.row_w != nullptr) p.row_w[row] = p.w[a];
   }
 }
 
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs
       const int row = excl[e] + rank;
       p.slot_row[a] = row;
       p.row_token[row] = t;
+      if (p.row_w != nullptr) p.row_w[row] = p.w[a];
     }
   }
 }

@@ -61,7 +61,7 @@ def gpu_route(cfg, T, logits=None, x=None, weights=None, ws=None):
     return idx, w, lo
 
 
-def gpu_permute(cfg, T, idx, w, x=None, ws=None):
+def gpu_permute(cfg, T, idx, w, x=None, ws=None, row_w=None):
     import mixture_experts_routing_sigmoid_b300 as moe
     A = T * cfg.top_k
     offsets = torch.empty(cfg.n_routed + 1, dtype=torch.int32, device="cuda")
@@ -72,7 +72,7 @@ def gpu_permute(cfg, T, idx, w, x=None, ws=None):
         x_perm = torch.zeros((max(A, 1), cfg.hidden), dtype=x.dtype, device="cuda")
     if ws is None:
         ws = workspace(cfg, T)
-    moe.moe_permute(cfg, T, idx, w, x, offsets, row_token, slot_row, x_perm, ws)
+    moe.moe_permute(cfg, T, idx, w, x, offsets, row_token, slot_row, x_perm, ws, row_w=row_w)
     assert moe.moe_get_error() == 0
     return offsets, row_token, slot_row, x_perm
 

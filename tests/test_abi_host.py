@@ -84,8 +84,8 @@ def test_null_and_misaligned_pointers_rejected(moe):
 def test_workspace_too_small_rejected(moe):
     cfg = CONFIGS["tiny"]
     c = moe.config_of(cfg)
-    st = moe.lib.moe_permute(ctypes.byref(c), 8, 0x1000, 0x2000, None, 0x3000, 0x4000, 0x5000,
-                             None, 0x6000, 64, None)
+    st = moe.lib.moe_permute(ctypes.byref(c), 8, 0x1000, 0x2000, None, 0x3000, 0x4000, None,
+                             0x5000, None, 0x6000, 64, None)
     assert st == moe.MOE_ERR_WORKSPACE
 
 

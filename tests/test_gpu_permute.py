@@ -28,14 +28,20 @@ def _check(cfg, T, idx, w, with_x=True):
         if cfg.capacity_drop else None
     offs_o, rt_o, sr_o = oracle.permute(cfg.replace(T=T), idx, kept)
     x = make_x(cfg, device="cuda", seed=9, T=T) if with_x else None
+    row_w = torch.full((max(T * cfg.top_k, 1),), float("nan"), device="cuda")
     offs, rt, sr, xp = gpu_permute(cfg, T, torch.from_numpy(idx).cuda(),
-                                   torch.from_numpy(w32).cuda(), x=x)
+                                   torch.from_numpy(w32).cuda(), x=x, row_w=row_w)
     np.testing.assert_array_equal(offs.cpu().numpy(), offs_o)
     R = int(offs_o[-1])
     np.testing.assert_array_equal(rt.cpu().numpy()[:R], rt_o)
     np.testing.assert_array_equal(sr.cpu().numpy()[:T * cfg.top_k], sr_o.ravel())
     if with_x and R:
         assert torch.equal(xp[:R], x[torch.from_numpy(rt_o).long().cuda()])
+    # row_w[r] is the routing weight of the assignment placed at row r
+    sr_flat = sr_o.ravel()
+    want = np.full(R, np.nan, dtype=np.float32)
+    want[sr_flat[sr_flat >= 0]] = w32.ravel()[sr_flat >= 0]
+    np.testing.assert_array_equal(row_w.cpu().numpy()[:R], want)
     return offs_o, kept
 
 
