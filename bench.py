@@ -158,17 +158,32 @@ def layer_work(cfg, counts, kept_rows: int) -> dict:
                 weight_bytes=(touched + S) * 3.0 * H * I * eb)
 
 
+def code_digest(path: str) -> str:
+    """sha256 of a source file's code with // comments and blank lines removed: a comment edit
+    keeps it, any change to the code does not."""
+    import hashlib
+    out = []
+    with open(path, encoding="utf-8") as fh:
+        for line in fh:
+            i = line.find("//")
+            if i >= 0:
+                line = line[:i]
+            line = line.rstrip()
+            if line.strip():
+                out.append(line)
+    return hashlib.sha256("\n".join(out).encode()).hexdigest()
+
+
 def traffic_per_launch(workload: str):
     """DRAM bytes (read + write) of one launch of the up GEMM on this workload, from the committed
-    ncu capture of that workload; None when there is no capture of it or the kernel source has
+    ncu capture of that workload; None when there is no capture of it or the kernel code has
     changed since the counters were taken."""
-    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     src = os.path.join(ROOT, "mixture_experts_routing_sigmoid_b300", "csrc", "gemm_tc.cu")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get("tc_gemm_kernel<MODE_UP>")
-    if not d or d.get("source_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
+    if not d or d.get("source_code_digest") != code_digest(src):
         return None
     c = d.get("captures", {}).get(workload)
     return None if c is None else float(c["dram_read_bytes"] + c["dram_write_bytes"])

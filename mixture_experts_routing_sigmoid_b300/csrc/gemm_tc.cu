@@ -29,9 +29,11 @@
 // each store instruction covering a contiguous run of one token's output row (neighbouring
 // lanes swap values to write bf16 pairs). No shared-memory staging.
 //
-// Persistent kernel, one 192-thread CTA per SM, CTA pairs take tiles round-robin in the order
-// problem by problem, weight tile by weight tile, token tile fastest (a segment's rows are
-// split into equal token tiles), so the pairs running together share weight tiles in L2.
+// Persistent kernel, one 224-thread CTA per SM. Tiles are numbered problem by problem (most
+// rows first), weight tile by weight tile, token tile fastest (a segment's rows are split into
+// equal token tiles). The first wave is one tile per CTA pair; after that a pair claims the next
+// index from a counter when its producer starts the current tile (round robin without a
+// counter), so the pairs sharing a weight tile run it together and its second read hits L2.
 //   warp 0      TMA producer (both CTAs): this CTA's weight rows and token rows of one k block
 //               per stage, 3-stage ring of 64 KB stages. A k block is 128 elements, two
 //               128-byte-swizzled units of 64 (one TMA box per operand and unit); when K / 64 is
@@ -44,6 +46,9 @@
 //               16, K=16; four per unit) into one of two 256-column fp32 accumulators.
 //   warps 2..5  epilogue (both CTAs): tcgen05.ld of the warp's 32 TMEM lanes, SwiGLU / router
 //               bias, stores.
+//   warp 6      tile scheduler: in the first CTA it claims, decodes and publishes each tile in
+//               the CTA's local ring and sends it to the second CTA by st.async; in the second
+//               CTA it relays the received tiles into that CTA's local ring.
 // Token columns past the segment end belong to the next expert (or lie beyond the tensor,
 // where TMA fills zeros); they are computed and never stored. Every mbarrier wait is bounded:
 // on timeout the CTA raises an abort flag and the device error word, drains, frees TMEM and
