@@ -10,8 +10,9 @@
 // One warp routes one token; lane l holds experts l, l+32, ... (coalesced loads of the
 // logit row). Keys are first evaluated in fp32. The chosen set then equals the exact (fp64)
 // one unless a decision margin (K-th vs (K+1)-th eligible key, Gk-th vs (Gk+1)-th group
-// score) lies within the fp32 error bound of the keys; such a token is redone in fp64 by the
-// same warp. For a softmax gate with no selection bias and max-based (or no) group scores the
+// score) lies within the fp32 error bound of the keys; such a token is rechecked by the same
+// warp: for a sigmoid gate only the groups and experts inside the error band are rescored in
+// fp64 (refine_sigmoid), otherwise the whole token is redone in fp64. For a softmax gate with no selection bias and max-based (or no) group scores the
 // logits themselves order the experts exactly (softmax is monotone), so no exp is needed.
 #include "common.cuh"
 #include "internal.h"
