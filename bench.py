@@ -407,14 +407,16 @@ def run_ours(args, world, rank, local):
 
     # ---- the oracle on the host cores (rank 0, N = 1 only), bounded sample
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = oracle_baseline(cfg, x, w, n_tokens=32, steps=1)
+        # about 10 s of host work: 8 timed passes over one 32-token sample
+        result["cpu_baseline"] = oracle_baseline(cfg, x, w, n_tokens=32, steps=1, repeat=8)
     return result
 
 
-def oracle_baseline(cfg, x, w, n_tokens: int, steps: int, seed: int = 0) -> dict:
-    """Time the fp64 oracle (as it stands) on `steps` samples of `n_tokens` tokens each.
+def oracle_baseline(cfg, x, w, n_tokens: int, steps: int, seed: int = 0, repeat: int = 1) -> dict:
+    """Time the fp64 oracle (as it stands) on `steps` samples of `n_tokens` tokens each, each
+    sample run `repeat` times (a longer timed span without staging more expert weights).
 
-    The experts a sample touches are copied to host memory before its timed call."""
+    The experts a sample touches are copied to host memory before its timed calls."""
     import numpy as np
     import torch
 
@@ -439,16 +441,18 @@ def oracle_baseline(cfg, x, w, n_tokens: int, steps: int, seed: int = 0) -> dict
             if ("r", int(e)) not in host:
                 host[("r", int(e))] = (w["w13"][int(e)].cpu(), w["w2"][int(e)].cpu())
         t0 = time.perf_counter()
-        if cfg.capacity_drop:
-            oracle.layer_forward(cfg, xs_all, wg, gb, sb, ew, sw, tokens=tok)
-        else:
-            oracle.layer_forward(cfg.replace(T=len(tok)), xr, wg, gb, sb, ew, sw)
+        for _ in range(repeat):
+            if cfg.capacity_drop:
+                oracle.layer_forward(cfg, xs_all, wg, gb, sb, ew, sw, tokens=tok)
+            else:
+                oracle.layer_forward(cfg.replace(T=len(tok)), xr, wg, gb, sb, ew, sw)
         total_s += time.perf_counter() - t0
-        total_tok += len(tok)
+        total_tok += len(tok) * repeat
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return {"value": total_tok / total_s, "unit": "tokens/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{steps} x {n_tokens} random tokens of the {cfg.name} batch: gate logits, "
+            "sample": f"{steps} x {n_tokens} random tokens of the {cfg.name} batch"
+                      + (f", each sample timed {repeat} times" if repeat > 1 else "") + ": gate logits, "
                       f"routing, {cfg.top_k} routed + {cfg.n_shared} shared SwiGLU experts and "
                       f"the combine in fp64 (touched expert weights staged in host memory)"
                       + ("; gate and routing over the whole batch for the drop"
