@@ -114,7 +114,10 @@ size_t moe_workspace_size(const moe_config* cfg, int32_t T);
  *   lower group); among their experts take the K highest keys (ties to the lower expert);
  *   w = s of the chosen experts (/ their sum if norm_topk) * routed_scale.
  * The chosen set is exactly the one exact (fp64) keys give: keys are evaluated in fp32, and a
- * token whose group or expert margin falls within the fp32 error bound is redone in fp64.
+ * token whose group or expert margin falls within the fp32 error bound is rechecked in fp64
+ * (for a sigmoid gate only the groups and experts inside the bound are rescored).
+ * ws (optional when logits_in is given) also holds the gate GEMM's split-K scratch for small
+ * batches; without it the gate runs unsplit.
  *   x          [T, H] dtype (unused if logits_in)
  *   logits_in  [T, N] fp32 or NULL;  logits_out [T, N] fp32 or NULL (written when computed)
  *   topk_idx   [T, K] int32 out: chosen experts in ascending expert index
