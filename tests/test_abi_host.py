@@ -100,3 +100,12 @@ def test_zero_tokens_is_a_no_op(moe):
     w = moe.MoeWeights()
     assert moe.lib.moe_layer_forward(ctypes.byref(c), 0, None, ctypes.byref(w), None, None, None,
                                      None, 0, None) == 0
+
+
+def test_permute_row_w_alignment_checked(moe):
+    cfg = CONFIGS["tiny"]
+    c = moe.config_of(cfg)
+    st = moe.lib.moe_permute(ctypes.byref(c), 8, 0x1000, 0x2000, None, 0x3000, 0x4000, 0x4004,
+                             0x5000, None, 0x6000, 1 << 30, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert "row_w" in moe.lib.moe_last_error_detail().decode()

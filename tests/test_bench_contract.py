@@ -50,3 +50,17 @@ def test_layer_work_counts_the_defined_flops_and_bytes():
     assert w["weight_bytes"] == (128 + S) * 3 * H * I * 2
     assert w["bytes"] == 2 * T * H * 2 + N * H * 2 + w["weight_bytes"] + T * N * 4 + T * K * 8
     assert bench.job_tokens_per_s(10.0, 4, 512, 5) == pytest.approx(4 * 512 * 5 / 0.010)
+
+
+def test_traffic_capture_keyed_by_code_not_comments(tmp_path):
+    """A committed DRAM-traffic capture stays valid across comment edits of the kernel source
+    and is dropped by any change to its code."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// header\nint f(int a) {  // add one\n  return a + 1;\n}\n")
+    d0 = bench.code_digest(str(src))
+    src.write_text("// another header\n\nint f(int a) {\n  return a + 1;  // still one\n}\n")
+    assert bench.code_digest(str(src)) == d0
+    src.write_text("int f(int a) {\n  return a + 2;\n}\n")
+    assert bench.code_digest(str(src)) != d0
