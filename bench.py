@@ -13,6 +13,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -25,6 +26,10 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s (route+permute+expert FFN+combine); % of roofline"
 # A timed region at least this long runs under the power cap: use the sustained bf16 peak.
 LONG_REGION_MS = 500.0
+# The oracle's CPU timing (both the cpu_baseline of our arm and every step of the reference
+# arm): samples of this many random tokens of the batch, each timed once.
+CPU_SAMPLE_TOKENS = 32
+CPU_SAMPLES = 16
 
 
 def parse():
@@ -158,35 +163,58 @@ def layer_work(cfg, counts, kept_rows: int) -> dict:
                 weight_bytes=(touched + S) * 3.0 * H * I * eb)
 
 
-def code_digest(path: str) -> str:
-    """sha256 of a source file's code with // comments and blank lines removed: a comment edit
-    keeps it, any change to the code does not."""
-    import hashlib
+GEMM_SOURCES = ("gemm_tc.cu", "common.cuh", "internal.h")
+
+
+def strip_comments(text: str) -> str:
+    """C/C++ source without // and /* */ comments (string literals with comment markers are not
+    expected in these files), blank lines and trailing spaces."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     out = []
-    with open(path, encoding="utf-8") as fh:
-        for line in fh:
-            i = line.find("//")
-            if i >= 0:
-                line = line[:i]
-            line = line.rstrip()
-            if line.strip():
-                out.append(line)
-    return hashlib.sha256("\n".join(out).encode()).hexdigest()
+    for line in text.splitlines():
+        i = line.find("//")
+        if i >= 0:
+            line = line[:i]
+        line = line.rstrip()
+        if line.strip():
+            out.append(line)
+    return "\n".join(out)
+
+
+def code_digest(*paths: str) -> str:
+    """sha256 over the code of the given source files (comments and blank lines removed): a
+    comment edit keeps it, any change to the code of any of the files does not."""
+    import hashlib
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, encoding="utf-8") as fh:
+            h.update(os.path.basename(path).encode() + b"\0")
+            h.update(strip_comments(fh.read()).encode() + b"\0")
+    return h.hexdigest()
+
+
+def gemm_digest() -> str:
+    """Digest of the code the tensor-core GEMM kernels are built from: the kernel file, the
+    inline-PTX helpers it includes and the argument layout it shares with the host."""
+    csrc = os.path.join(ROOT, "mixture_experts_routing_sigmoid_b300", "csrc")
+    return code_digest(*(os.path.join(csrc, f) for f in GEMM_SOURCES))
 
 
 def traffic_per_launch(workload: str):
     """DRAM bytes (read + write) of one launch of the up GEMM on this workload, from the committed
     ncu capture of that workload; None when there is no capture of it or the kernel code has
-    changed since the counters were taken."""
+    changed since the counters were taken. A capture taken on a smaller case of the same kernel
+    carries its scale factor to the full launch (`scale_to`)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "mixture_experts_routing_sigmoid_b300", "csrc", "gemm_tc.cu")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get("tc_gemm_kernel<MODE_UP>")
-    if not d or d.get("source_code_digest") != code_digest(src):
+    if not d or d.get("source_code_digest") != gemm_digest():
         return None
     c = d.get("captures", {}).get(workload)
-    return None if c is None else float(c["dram_read_bytes"] + c["dram_write_bytes"])
+    if c is None:
+        return None
+    return float(c["dram_read_bytes"] + c["dram_write_bytes"]) * float(c.get("scale_to", 1.0))
 
 
 def workload_name(cfg) -> str:
@@ -407,8 +435,10 @@ def run_ours(args, world, rank, local):
 
     # ---- the oracle on the host cores (rank 0, N = 1 only), bounded sample
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # about 10 s of host work: 8 timed passes over one 32-token sample
-        result["cpu_baseline"] = oracle_baseline(cfg, x, w, n_tokens=32, steps=1, repeat=8)
+        # about 10 s of host work: CPU_SAMPLES samples of CPU_SAMPLE_TOKENS tokens each, the
+        # same per-sample recipe as the reference arm's steps
+        result["cpu_baseline"] = oracle_baseline(cfg, x, w, n_tokens=CPU_SAMPLE_TOKENS,
+                                                 steps=CPU_SAMPLES, seed=1)
     return result
 
 
@@ -454,7 +484,8 @@ def oracle_baseline(cfg, x, w, n_tokens: int, steps: int, seed: int = 0, repeat:
             "sample": f"{steps} x {n_tokens} random tokens of the {cfg.name} batch"
                       + (f", each sample timed {repeat} times" if repeat > 1 else "") + ": gate logits, "
                       f"routing, {cfg.top_k} routed + {cfg.n_shared} shared SwiGLU experts and "
-                      f"the combine in fp64 (touched expert weights staged in host memory)"
+                      f"the combine in fp64; the expert weights a sample touches are staged in "
+                      f"host memory before its timed call (staging not timed)"
                       + ("; gate and routing over the whole batch for the drop"
                          if cfg.capacity_drop else ""),
             "seconds": total_s}
@@ -469,10 +500,10 @@ def run_reference(args, world, rank, local):
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     w = make_weights(cfg, device=dev, seed=0)
     x = make_x(cfg, device=dev, seed=0)
-    n_tok = 4
     if args.warmup:
-        oracle_baseline(cfg, x, w, n_tokens=n_tok, steps=1, seed=99)
-    cb = oracle_baseline(cfg, x, w, n_tokens=n_tok, steps=args.steps, seed=1)
+        oracle_baseline(cfg, x, w, n_tokens=CPU_SAMPLE_TOKENS, steps=1, seed=99)
+    # one step = one sample of CPU_SAMPLE_TOKENS tokens, as in our arm's cpu_baseline
+    cb = oracle_baseline(cfg, x, w, n_tokens=CPU_SAMPLE_TOKENS, steps=args.steps, seed=1)
     ms_step = cb["seconds"] / args.steps * 1e3
     return {"metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

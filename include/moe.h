@@ -166,8 +166,9 @@ moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_idx
  *   Limits: T <= 65536 (larger T returns MOE_ERR_UNSUPPORTED), n_routed <= 256, n_groups <= 32.
  *   All calls share that array: calls that overlap on the GPU race and give wrong results.
  *   Nothing in it needs clearing between calls (each call writes what it reads).
- *   The first call on a device looks up the array's device address (once per device, with
- *   that device current); make it before any stream capture. No allocation happens, ever.
+ *   The first call on a device looks up the array's device address (with that device
+ *   current), and so does the first call after the device's context changed (a device reset);
+ *   make those calls before any stream capture. No allocation happens, ever.
  */
 moe_status moe_permute_static_scratch(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
                                       const float* topk_w, const void* x, int32_t* offsets,

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <atomic>
+#include <mutex>
 #include <new>
 
 #include "../../include/moe.h"
@@ -29,16 +30,12 @@ moe_status fail(moe_status s, const char* fmt, ...) {
 // Per-device error word (one int per device that has used the library).
 __device__ int g_error_word[1];
 
+std::mutex g_symbol_mutex;
+
 int* error_word() {
-  static int* ptr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    ptr[dev] = static_cast<int*>(p);
-  }
-  return ptr[dev];
+  static moe::SymbolCache cache;
+  std::lock_guard<std::mutex> lock(g_symbol_mutex);
+  return static_cast<int*>(cache.get(g_error_word));
 }
 
 int num_sms() {
@@ -386,6 +383,23 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
 
 // Accessors for other entry-point files of this library (same checks, same error reporting).
 namespace moe {
+
+uintptr_t current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static const Fn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<Fn>(p);
+    return static_cast<Fn>(nullptr);
+  }();
+  CUcontext ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return 0;
+  return reinterpret_cast<uintptr_t>(ctx);
+}
+
 namespace {
 std::atomic<unsigned long long> g_launches{0};
 }

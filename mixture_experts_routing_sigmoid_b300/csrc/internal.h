@@ -137,6 +137,33 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st);
 // fp32 on CUDA cores (gemm_simt.cu)
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t st);
 
+// Handle of the CUDA context current on the calling thread (0 if none or unknown). A device
+// address looked up with cudaGetSymbolAddress belongs to that context: after a device reset
+// (a new primary context) the old address is dead, so caches of such addresses key on it.
+uintptr_t current_context();
+
+// Device address of a __device__ variable on the current device, looked up once per device and
+// context and cached (nullptr if the lookup failed). Not thread-safe: callers serialise.
+struct SymbolCache {
+  void* ptr[64] = {nullptr};
+  uintptr_t ctx[64] = {0};
+  template <typename Sym>
+  void* get(const Sym& symbol) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    const uintptr_t now = current_context();
+    if (ptr[dev] != nullptr && now != 0 && now == ctx[dev]) return ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) {
+      ptr[dev] = nullptr;
+      return nullptr;
+    }
+    ptr[dev] = p;
+    ctx[dev] = current_context();  // the lookup made the device's primary context current
+    return p;
+  }
+};
+
 // Shared argument checking and error reporting of the C ABI (abi.cu).
 }  // namespace moe
 #include "../../include/moe.h"

@@ -16,9 +16,9 @@
 // different host threads without ordering) race on it and give wrong results. Nothing in the
 // array has to start at zero: each call writes every scratch word before it reads it.
 //
-// The device address of the array is looked up once per device (cudaGetSymbolAddress, with that
-// device current) on the first call made on that device; make that first call before any
-// stream capture.
+// The device address of the array is looked up (cudaGetSymbolAddress, with the device current)
+// on the first call made on each device, and again on the first call after that device's
+// context has changed (a device reset); make those calls before any stream capture.
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -43,24 +43,17 @@ static_assert(kMaskBytes % 256 == 0 && kCountBytes % 256 == 0, "regions stay 256
 static __device__ __align__(256) unsigned char g_permute_scratch[kScratchBytes];
 
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[64] = {nullptr};
 
-// Device address of g_permute_scratch on the current device (looked up once per device).
+// Device address of g_permute_scratch on the current device, looked up on the first call on
+// each device (cudaGetSymbolAddress with that device current) and again whenever the device's
+// context has changed since (after a device reset the old address is dead).
 moe_status scratch_on_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return moe::abi_cuda_status(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return moe::abi_fail(MOE_ERR_UNSUPPORTED, "device index >= 64");
+  static moe::SymbolCache cache;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess || p == nullptr)
-      return moe::abi_cuda_status(e == cudaSuccess ? cudaErrorInvalidSymbol : e,
-                                  "cudaGetSymbolAddress(permute scratch)");
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = cache.get(g_permute_scratch);
+  if (p == nullptr)
+    return moe::abi_fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(permute scratch) failed");
+  *out = p;
   return MOE_OK;
 }
 

@@ -53,14 +53,22 @@ def test_layer_work_counts_the_defined_flops_and_bytes():
 
 
 def test_traffic_capture_keyed_by_code_not_comments(tmp_path):
-    """A committed DRAM-traffic capture stays valid across comment edits of the kernel source
-    and is dropped by any change to its code."""
+    """A committed DRAM-traffic capture stays valid across comment edits of the kernel sources
+    (// and /* */) and is dropped by any change to the code of any of them."""
     sys.path.insert(0, ROOT)
     import bench
-    src = tmp_path / "k.cu"
+    src, hdr = tmp_path / "k.cu", tmp_path / "h.cuh"
     src.write_text("// header\nint f(int a) {  // add one\n  return a + 1;\n}\n")
-    d0 = bench.code_digest(str(src))
+    hdr.write_text("/* helper */\nint g(int b) { return b * 2; }\n")
+    d0 = bench.code_digest(str(src), str(hdr))
     src.write_text("// another header\n\nint f(int a) {\n  return a + 1;  // still one\n}\n")
-    assert bench.code_digest(str(src)) == d0
+    hdr.write_text("/* a helper,\n   over two lines */\nint g(int b) { return b * 2; }\n")
+    assert bench.code_digest(str(src), str(hdr)) == d0
+    hdr.write_text("int g(int b) { return /* doubled */ b * 3; }\n")
+    assert bench.code_digest(str(src), str(hdr)) != d0
+    hdr.write_text("/* helper */\nint g(int b) { return b * 2; }\n")
     src.write_text("int f(int a) {\n  return a + 2;\n}\n")
-    assert bench.code_digest(str(src)) != d0
+    assert bench.code_digest(str(src), str(hdr)) != d0
+    # the GEMM digest covers the kernel file, its PTX helpers and the shared argument layout
+    assert set(bench.GEMM_SOURCES) == {"gemm_tc.cu", "common.cuh", "internal.h"}
+    assert len(bench.gemm_digest()) == 64

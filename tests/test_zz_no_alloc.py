@@ -4,7 +4,9 @@ Such callers (an allocator-free runtime, a plugin whose host framework owns ever
 allocation, a process that must not grow its device footprint) cannot pass a workspace, so
 this entry point keeps its scratch in a 2.5 MiB device array inside the library. Its outputs
 must equal moe_permute's bit for bit (integer index work), call after call: the array keeps the
-previous call's contents, so two different calls in a row are compared.
+previous call's contents, so two different calls in a row are compared. The largest case is
+the documented cap (65536 tokens, 256 experts), where every region of the array is in use; it
+permutes indices only.
 This file is collected last on purpose; it also passes when run on its own.
 """
 import ctypes
@@ -36,7 +38,8 @@ def _outputs(cfg, T, with_x):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("cfg", [MID_V2, MID_A, CONFIGS["v2"], CONFIGS["v3_prefill"]],
+@pytest.mark.parametrize("cfg", [MID_V2, MID_A, CONFIGS["v2"], CONFIGS["v3_prefill"],
+                                 CONFIGS["v3_prefill"].replace(name="v3_t65536", T=65536)],
                          ids=lambda c: c.name)
 def test_static_scratch_permute_matches_workspace_permute(cfg):
     import mixture_experts_routing_sigmoid_b300 as moe
