@@ -201,6 +201,20 @@ moe_status moe_expert_down(const moe_config* cfg, int32_t T, const void* h,
                            void* y_perm, void* y_shared, moe_stream_t stream);
 
 /*
+ * The up half with its routed rows read straight from x in token order ([P4] section 5's
+ * dispatch done as a row gather inside the GEMM instead of a copy): row r of expert e's
+ * segment is x[row_token[r]]. This is what moe_layer_forward runs on the bf16 path, so that
+ * the permuted copy x_perm is never written or read. Outputs are bitwise equal to
+ * moe_expert_up's on x_perm = x[row_token]. bf16 only (MOE_ERR_UNSUPPORTED for fp32).
+ *   x [T, H] bf16;  row_token [T*K] int32 and offsets [N+1] int32 from moe_permute (values are
+ *   clamped to [0, T-1] on the device);  h, h_shared as for moe_expert_up.
+ */
+moe_status moe_expert_up_gather(const moe_config* cfg, int32_t T, const void* x,
+                                const int32_t* row_token, const int32_t* offsets,
+                                const moe_weights* w, void* h, void* h_shared,
+                                moe_stream_t stream);
+
+/*
  * Weighted combine back to token order ([P2] section 2.2 forward):
  *   out[t] = sum_k [slot_row(t,k) >= 0] topk_w[t,k] y_perm[slot_row(t,k)] + y_shared[t]
  *   (fp32 accumulation; y_shared may be NULL). out [T, H] dtype.
@@ -269,8 +283,9 @@ moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float r
  * this process records a CUDA event on its stream at the start of every stage and at its end;
  * nothing synchronises inside the calls. Stages, in order:
  *   0 gate GEMM, 1 routing, 2 load statistics (zero when not requested), 3 permutation
- *   (drop thresholds, histogram, scan, scatter), 4 row dispatch (x -> x_perm), 5 expert up
- *   GEMM (routed + shared, SwiGLU), 6 expert down GEMM, 7 combine.
+ *   (drop thresholds, histogram, scan, scatter), 4 row dispatch (x -> x_perm; empty on the
+ *   bf16 path, where the up GEMM gathers its rows from x), 5 expert up GEMM (routed + shared,
+ *   SwiGLU), 6 expert down GEMM, 7 combine.
  * Calls captured into a CUDA graph record their events as graph nodes, which record each time
  * the graph runs; stop then reads the last run's times.
  * moe_stage_timing_start creates the events (host resources only, no device memory).

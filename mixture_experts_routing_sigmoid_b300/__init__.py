@@ -13,8 +13,8 @@ import os
 
 __all__ = ["MoeError", "MoeConfig", "MoeWeights", "lib", "make_config", "make_weights",
            "moe_workspace_size", "moe_route", "moe_load_stats", "moe_permute",
-           "moe_expert_ffn", "moe_expert_up", "moe_expert_down", "moe_combine",
-           "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
+           "moe_expert_ffn", "moe_expert_up", "moe_expert_up_gather", "moe_expert_down",
+           "moe_combine", "moe_layer_forward", "moe_get_error", "moe_selftest_wait_timeout",
            "moe_status_string", "moe_permute_static_scratch", "moe_stage_timing_start",
            "moe_stage_timing_stop", "moe_bias_update", "moe_seq_balance_loss", "moe_kernel_launches", "moe_group_balance_losses",
            "moe_plan_placement", "MoePlacementConfig", "STAGE_NAMES", "EXPORTED_SYMBOLS", "LIB_PATH", "MOE_OK", "MOE_ERR_INVALID_ARG",
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_load_stats", "moe_pe
                     "moe_status_string", "moe_last_error_detail", "moe_permute_static_scratch",
                     "moe_stage_timing_start", "moe_stage_timing_stop", "moe_bias_update",
                     "moe_seq_balance_loss", "moe_kernel_launches", "moe_group_balance_losses",
-                    "moe_plan_placement")
+                    "moe_plan_placement", "moe_expert_up_gather")
 
 # Stages of moe_layer_forward as moe_stage_timing_stop reports them (MOE_N_STAGES).
 STAGE_NAMES = ("gate", "route", "stats", "permute", "dispatch", "up", "down", "combine")
@@ -84,6 +84,7 @@ def _load():
         "moe_permute_static_scratch": (I32, [CFG, I32, P, P, P, P, P, P, P, P]),
         "moe_expert_ffn": (I32, [CFG, I32, P, P, P, W, P, P, P, SZ, P]),
         "moe_expert_up": (I32, [CFG, I32, P, P, P, W, P, P, P]),
+        "moe_expert_up_gather": (I32, [CFG, I32, P, P, P, W, P, P, P]),
         "moe_expert_down": (I32, [CFG, I32, P, P, P, W, P, P, P]),
         "moe_combine": (I32, [CFG, I32, P, P, P, P, P, P]),
         "moe_layer_forward": (I32, [CFG, I32, P, W, P, P, P, P, SZ, P]),
@@ -221,6 +222,12 @@ def moe_expert_up(cfg, T, x_perm, offsets, x, weights, h, h_shared, stream=None)
     _check(lib.moe_expert_up(ctypes.byref(_cfg(cfg)), int(T), _ptr(x_perm), _ptr(offsets),
                              _ptr(x), ctypes.byref(_w(weights)), _ptr(h), _ptr(h_shared),
                              _stream(stream)), "moe_expert_up")
+
+
+def moe_expert_up_gather(cfg, T, x, row_token, offsets, weights, h, h_shared, stream=None):
+    _check(lib.moe_expert_up_gather(ctypes.byref(_cfg(cfg)), int(T), _ptr(x), _ptr(row_token),
+                                    _ptr(offsets), ctypes.byref(_w(weights)), _ptr(h),
+                                    _ptr(h_shared), _stream(stream)), "moe_expert_up_gather")
 
 
 def moe_expert_down(cfg, T, h, offsets, h_shared, weights, y_perm, y_shared, stream=None):

@@ -97,6 +97,9 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
 
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Largest batch whose routed rows the layer's up projection gathers from x (see layer_steps).
+constexpr int32_t kGatherMaxTokens = 32;
+
 // Workspace carve for one config and token count. Every region is 256-byte aligned.
 struct Layout {
   size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_lse,
@@ -253,10 +256,11 @@ moe_status do_stats(const moe_config* c, int32_t T, const float* u, const int32_
   return cuda_status(launch_stats(s, st), "load stats");
 }
 
+// x_perm == nullptr: the permutation only (no row copies; the up GEMM then gathers its rows).
 moe_status do_permute(const moe_config* c, int32_t T, const int32_t* idx, const float* wt,
                       const void* x, int32_t* offsets, int32_t* row_token, float* row_w,
                       int32_t* slot_row,
-                      void* x_perm, void* ws, cudaStream_t st) {
+                      void* x_perm, void* ws, cudaStream_t st, int32_t* sched_zero = nullptr) {
   const Layout L = layout(c, T);
   PermuteArgs p;
   p.T = T; p.N = c->n_routed; p.K = c->top_k; p.D = c->n_groups;
@@ -268,6 +272,7 @@ moe_status do_permute(const moe_config* c, int32_t T, const int32_t* idx, const 
   p.cnt = at<int32_t>(ws, L.cnt);
   p.base = at<int32_t>(ws, L.base);
   p.thr = at<unsigned long long>(ws, L.thr);
+  p.sched_zero = sched_zero;
   p.err = error_word();
   TRY_S(cuda_status(launch_permute(p, num_sms(), st), "permute"));
   stage_mark(STAGE_DISPATCH, st);
@@ -282,18 +287,20 @@ moe_status reset_sched(const moe_config* c, int32_t T, void* ws, cudaStream_t st
 }
 
 // sched: the two tile counters (up, down) zeroed by reset_sched, or nullptr (static schedule).
+// row_token != nullptr (bf16 only): the routed rows are gathered from x (x_perm unused).
 moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32_t* offsets,
                  const void* x, const moe_weights* w, void* h, void* h_sh, int32_t* sched,
-                 cudaStream_t st) {
+                 cudaStream_t st, const int32_t* row_token = nullptr) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_UP;
   g.T = T; g.H = c->hidden; g.I = c->inter; g.S = c->n_shared; g.N = c->n_routed;
   g.n_routed = c->n_routed; g.has_shared = c->n_shared > 0 ? 1 : 0;
   g.offsets = offsets; g.rows_cap = T * c->top_k;
-  g.a0 = x_perm; g.a1 = x; g.b0 = w->w13; g.b1 = w->w13_shared;
+  g.a0 = row_token != nullptr ? x : x_perm; g.a1 = x; g.b0 = w->w13; g.b1 = w->w13_shared;
   g.out0 = h; g.out1 = h_sh; g.err = error_word();
   g.sched = sched;
+  g.row_token = row_token;
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "expert up GEMM");
 }
@@ -367,12 +374,20 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
   stage_mark(STAGE_STATS, st);
   if (counts != nullptr || lb_z != nullptr)
     TRY(do_stats(cfg, T, u, idx, counts, nullptr, nullptr, lb_z, ws, st));
-  stage_mark(STAGE_PERMUTE, st);
-  TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, nullptr, slot_row, xy, ws, st));
+  // Batches of at most 32 tokens (bf16): every expert segment has at most 32 rows, and the up
+  // GEMM gathers them straight from x through row_token (tile::gather4 loads) at the speed of
+  // contiguous loads, so the x_perm copy is skipped (the dispatch stage stays empty). Larger
+  // segments load contiguous x_perm rows: a row gather issues one load per four rows, and with
+  // hundreds of token rows per tile those loads, not the memory, bound the GEMM.
+  const bool gather = cfg->dtype == MOE_BF16 && T <= kGatherMaxTokens;
+  // the permutation also zeroes the expert GEMMs' tile counters (no memset between the kernels,
+  // so each kernel can start while the one ahead of it finishes)
   int32_t* sched = at<int32_t>(ws, L.sched);
+  stage_mark(STAGE_PERMUTE, st);
+  TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, nullptr, slot_row,
+                 gather ? nullptr : xy, ws, st, sched));
   stage_mark(STAGE_UP, st);
-  TRY(reset_sched(cfg, T, ws, st));
-  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, sched, st));
+  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, sched, st, gather ? row_token : nullptr));
   stage_mark(STAGE_DOWN, st);
   TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, sched, st));  // y_perm overwrites x_perm
   stage_mark(STAGE_COMBINE, st);
@@ -504,6 +519,24 @@ moe_status moe_expert_up(const moe_config* cfg, int32_t T, const void* x_perm,
     CHECK_PTR(h_shared);
   }
   return do_up(cfg, T, x_perm, offsets, x, w, h, h_shared, nullptr, S_(stream));
+}
+
+moe_status moe_expert_up_gather(const moe_config* cfg, int32_t T, const void* x,
+                                const int32_t* row_token, const int32_t* offsets,
+                                const moe_weights* w, void* h, void* h_shared,
+                                moe_stream_t stream) {
+  g_detail[0] = 0;
+  TRY(check_cfg(cfg, T));
+  if (T == 0) return MOE_OK;
+  if (cfg->dtype != MOE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "the row gather runs on the bf16 tensor-core path only");
+  TRY(check_weights(cfg, w, false, true));
+  CHECK_PTR(x);
+  CHECK_PTR(row_token);
+  CHECK_PTR(offsets);
+  CHECK_PTR(h);
+  if (cfg->n_shared > 0) CHECK_PTR(h_shared);
+  return do_up(cfg, T, nullptr, offsets, x, w, h, h_shared, nullptr, S_(stream), row_token);
 }
 
 moe_status moe_expert_down(const moe_config* cfg, int32_t T, const void* h,

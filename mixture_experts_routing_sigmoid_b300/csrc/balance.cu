@@ -21,6 +21,8 @@ namespace moe {
 namespace {
 
 __global__ void __launch_bounds__(256) bias_update_kernel(BiasUpdateArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ long long part[8];
   long long s = 0;
   for (int e = threadIdx.x; e < a.N; e += blockDim.x) s += a.counts[e];
@@ -40,6 +42,8 @@ __global__ void __launch_bounds__(256) bias_update_kernel(BiasUpdateArgs a) {
 constexpr int MAXJ = 8;  // experts per lane (N <= 256)
 
 __global__ void __launch_bounds__(256) seq_partial_kernel(SeqLossArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8][256];
   __shared__ int cnt[256];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -101,6 +105,8 @@ __global__ void __launch_bounds__(256) seq_partial_kernel(SeqLossArgs a) {
 }
 
 __global__ void __launch_bounds__(256) seq_final_kernel(SeqLossArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ double colsum[256];
   __shared__ double fp[256];
   const int b = blockIdx.x, e = threadIdx.x;
@@ -134,6 +140,8 @@ __global__ void __launch_bounds__(256) seq_final_kernel(SeqLossArgs a) {
 }
 
 __global__ void seq_mean_kernel(SeqLossArgs a) {
+  pdl_wait();
+  pdl_trigger();
   double s = 0.0;
   for (int b = 0; b < a.B; ++b) s += a.seq_lb[b];
   a.mean[0] = (float)(s / a.B);
@@ -148,17 +156,15 @@ int seq_loss_chunks(int L) {
 
 cudaError_t launch_seq_loss(const SeqLossArgs& a, cudaStream_t st) {
   if (a.B <= 0) return cudaSuccess;
-  seq_partial_kernel<<<dim3(a.B, a.cps), 256, 0, st>>>(a);
-  seq_final_kernel<<<a.B, 256, 0, st>>>(a);
-  seq_mean_kernel<<<1, 1, 0, st>>>(a);
-  note_launches(3);
+  cudaError_t e = launch_pdl(seq_partial_kernel, dim3(a.B, a.cps), dim3(256), 0, st, a);
+  if (e == cudaSuccess) e = launch_pdl(seq_final_kernel, dim3(a.B), dim3(256), 0, st, a);
+  if (e == cudaSuccess) e = launch_pdl(seq_mean_kernel, dim3(1), dim3(1), 0, st, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_bias_update(const BiasUpdateArgs& a, cudaStream_t st) {
-  bias_update_kernel<<<1, 256, 0, st>>>(a);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(bias_update_kernel, dim3(1), dim3(256), 0, st, a);
 }
 
 }  // namespace moe

@@ -15,6 +15,8 @@ namespace {
 
 template <typename T, int KC>  // KC = top_k (compile time), or 0 for any K <= 16
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int V = Vec<T>::N;
   constexpr int KM = KC > 0 ? KC : 16;
   const int K = KC > 0 ? KC : a.K;
@@ -67,14 +69,13 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 }
 
 template <typename T>
-void launch_typed(const CombineArgs& a, int blocks, cudaStream_t st) {
+cudaError_t launch_typed(const CombineArgs& a, int blocks, cudaStream_t st) {
   switch (a.K) {
-    case 4: combine_kernel<T, 4><<<blocks, 256, 0, st>>>(a); break;
-    case 6: combine_kernel<T, 6><<<blocks, 256, 0, st>>>(a); break;
-    case 8: combine_kernel<T, 8><<<blocks, 256, 0, st>>>(a); break;
-    default: combine_kernel<T, 0><<<blocks, 256, 0, st>>>(a); break;
+    case 4: return launch_pdl(combine_kernel<T, 4>, dim3(blocks), dim3(256), 0, st, a);
+    case 6: return launch_pdl(combine_kernel<T, 6>, dim3(blocks), dim3(256), 0, st, a);
+    case 8: return launch_pdl(combine_kernel<T, 8>, dim3(blocks), dim3(256), 0, st, a);
+    default: return launch_pdl(combine_kernel<T, 0>, dim3(blocks), dim3(256), 0, st, a);
   }
-  note_launches(1);
 }
 
 }  // namespace
@@ -85,11 +86,8 @@ cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st) {
   const size_t n = (size_t)a.T * (a.H / V);
   size_t blocks = (n + 255) / 256;
   if (blocks > (size_t)num_sms * 16) blocks = (size_t)num_sms * 16;
-  if (a.dtype == 1)
-    launch_typed<__nv_bfloat16>(a, (int)blocks, st);
-  else
-    launch_typed<float>(a, (int)blocks, st);
-  return cudaGetLastError();
+  return a.dtype == 1 ? launch_typed<__nv_bfloat16>(a, (int)blocks, st)
+                      : launch_typed<float>(a, (int)blocks, st);
 }
 
 }  // namespace moe

@@ -66,6 +66,17 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v) {
                :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// ------------------------------------------------------------------ dependent launches
+// A kernel launched with programmatic stream serialization may start before the kernel ahead of
+// it in the stream has finished. pdl_wait() blocks until that kernel has completed and its
+// memory operations are visible (a no-op for a normal launch): every kernel of this library calls
+// it before its first access to global memory other than its own parameters. pdl_trigger() lets
+// the next kernel in the stream start launching (its CTAs then wait in their own pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ timers, shared memory
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -283,6 +294,21 @@ __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const void* tmap,
       " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1),
          "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+// Row gather (tile::gather4) into this CTA's shared memory: rows r0, r1, r2, r3 of a 2-D
+// tensor whose map has a box one row high, columns c0 .. c0 + box width - 1, written as four
+// consecutive box rows at dst (the layout a 4-row tiled box would have there; with a swizzled
+// map the pattern follows the shared-memory address as for tiled loads). Completion counted as
+// for tma_load_2d_pair.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const void* tmap,
+                                                 uint32_t bar_cluster, int c0, int r0, int r1,
+                                                 int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(r0),
+         "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 // TMEM allocation shared by the CTA pair: one warp of EACH CTA executes it.

@@ -53,6 +53,8 @@ __device__ __forceinline__ float wval(const GemmArgs& a, int p, bool shared, int
 }
 
 __global__ void __launch_bounds__(256) simt_gemm_kernel(GemmArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int p = blockIdx.z;
   const Prob q = get_prob(a, p);
   const int m0 = blockIdx.y * TM;
@@ -152,9 +154,7 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t st) {
   if (probs == 0) return cudaSuccess;
   // routed rows of one expert never exceed T (a token picks an expert at most once)
   dim3 grid((ncols_max + TN - 1) / TN, (a.T + TM - 1) / TM, probs);
-  simt_gemm_kernel<<<grid, 256, 0, st>>>(a);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm_kernel, grid, dim3(256), 0, st, a);
 }
 
 }  // namespace moe

@@ -86,6 +86,8 @@ struct TcParams {
   CUtensorMap tmW0, tmW1;    // weights: routed, shared (box 128 rows; UP: interleaved 5-D box)
   CUtensorMap tmX0, tmX1;    // tokens: routed, shared (box 64 rows)
   CUtensorMap tmX0s, tmX1s;  // tokens: routed, shared (box 32 rows)
+  CUtensorMap tmXg;          // UP with row gather: x [T, H], box one row high (tile::gather4)
+  const int32_t* row_token;  // UP with row gather: token of each routed row, else nullptr
   const int32_t* offsets;
   int n_routed, has_shared, T, H, I, S, N;
   void* out0;
@@ -131,6 +133,7 @@ struct SmemCtl {
   uint64_t took;               // first CTA: its producer has started the last published tile
   Tile lsq[SQ];
   Tile xq[SQ];
+  int grow[SQ][TOK / 2];      // row gather: x row of each of this CTA's token rows of lsq[slot]
   uint32_t tmem_base;
   int abort_flag;
   int nprob;
@@ -321,11 +324,32 @@ __device__ __forceinline__ void lds_tile(uint32_t a, Tile& t) {
                  : "=r"(w[i]), "=r"(w[i + 1]), "=r"(w[i + 2]), "=r"(w[i + 3]) : "r"(a + 4 * i) : "memory");
 }
 
-// Publish `t` in slot `qs` of this CTA's local ring. Warp-wide (producer warp).
+// Row gather: the x row of each of this CTA's token rows of tile t (rows t.r0 + rank * ncols/2
+// ..), into slot qs's row list. Rows past the tile's stored rows (MMA padding, never stored)
+// take the tile's first token. Warp-wide.
+__device__ __forceinline__ void fill_rows(SmemCtl& c, uint32_t qs, const TcParams& p,
+                                          const Tile& t, uint32_t rank) {
+  const int half = t.ncols / 2;
+  const int base = t.r0 + (int)rank * half;
+  const int end = t.r0 + t.nrows;
+  const int pad = __ldg(p.row_token + t.r0);
+  for (int i = threadIdx.x & 31; i < half; i += 32) {
+    const int r = base + i;
+    const int tok = r < end ? __ldg(p.row_token + r) : pad;
+    c.grow[qs][i] = min(max(tok, 0), p.T - 1);
+  }
+  __threadfence_block();
+  __syncwarp();
+}
+
+// Publish `t` in slot `qs` of this CTA's local ring (with its gathered rows when gp is given).
+// Warp-wide (scheduler warp).
 __device__ __forceinline__ bool ring_publish(SmemCtl& c, uint32_t qs, uint32_t qph, const Tile& t,
-                                             volatile int* abort_flag, int* err) {
+                                             volatile int* abort_flag, int* err,
+                                             const TcParams* gp = nullptr, uint32_t rank = 0) {
   if (!warp_wait_bounded(smem_u32(&c.lempty[qs]), qph ^ 1u, abort_flag, err, TIMEOUT_NS))
     return false;
+  if (gp != nullptr && t.prob >= 0 && !t.shared) fill_rows(c, qs, *gp, t, rank);
   if ((threadIdx.x & 31) == 0) {
     sts_tile(smem_u32(&c.lsq[qs]), t);
     mbar_arrive(smem_u32(&c.lfull[qs]));
@@ -380,11 +404,14 @@ __device__ __forceinline__ bool ring_take(SmemCtl& c, uint32_t qs, uint32_t qph,
   return true;
 }
 
-// Warp-wide ring_take: lane 0 waits, every lane reads the slot, lane 0 releases it.
+// Warp-wide ring_take: lane 0 waits, every lane reads the slot, lane 0 releases it. With
+// `rows`, lane l also takes gathered rows 4l .. 4l+3 of the slot.
 __device__ __forceinline__ bool ring_take_warp(SmemCtl& c, uint32_t qs, uint32_t qph, Tile& t,
-                                               volatile int* abort_flag, int* err) {
+                                               volatile int* abort_flag, int* err,
+                                               int4* rows = nullptr) {
   if (!warp_wait_bounded(smem_u32(&c.lfull[qs]), qph, abort_flag, err, TIMEOUT_NS)) return false;
   lds_tile(smem_u32(&c.lsq[qs]), t);
+  if (rows != nullptr) *rows = *reinterpret_cast<const int4*>(&c.grow[qs][4 * (threadIdx.x & 31)]);
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&c.lempty[qs]));
   return true;
@@ -425,6 +452,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(&c.tmem_base), TMEM_COLS);
 
+  // the kernel ahead in the stream (permutation, or the up projection for the down one) has
+  // finished and its writes are visible from here on
+  pdl_wait();
+  pdl_trigger();
   // ---- problems in order of decreasing rows, so that the longest run first and the pairs
   // finish together; then the tile prefix over that order (counts depend on device offsets)
   const int nprob = (MODE == MODE_GATE) ? 1 : p.n_routed + p.has_shared;
@@ -481,10 +512,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 
   if (warp == 0) {
     // ================================================================ TMA producer
+    const bool gather = MODE == MODE_UP && p.row_token != nullptr;
     if (lane == 0) {
       tma_prefetch_desc(&p.tmW0);
-      tma_prefetch_desc(&p.tmX0);
-      tma_prefetch_desc(&p.tmX0s);
+      if (gather) {
+        tma_prefetch_desc(&p.tmXg);
+      } else {
+        tma_prefetch_desc(&p.tmX0);
+        tma_prefetch_desc(&p.tmX0s);
+      }
       if (MODE != MODE_GATE && p.has_shared) {
         tma_prefetch_desc(&p.tmW1);
         tma_prefetch_desc(&p.tmX1);
@@ -497,13 +533,47 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     bool ok = true;
     while (ok) {
       Tile t;
-      if (!ring_take_warp(c, qs, qph, t, abort_flag, p.err)) {
+      int4 rows;  // row gather: this lane's four x rows
+      if (!ring_take_warp(c, qs, qph, t, abort_flag, p.err, gather ? &rows : nullptr)) {
         ok = false;
         break;
       }
       if (++qs == SQ) { qs = 0; qph ^= 1u; }
       if (t.prob < 0) break;
       if (rank == 0 && lane == 0) mbar_arrive(bar(c.took));  // the scheduler may claim the next
+      if (gather && !t.shared) {
+        // routed rows gathered from x: lanes 0 / 1 load the weight box of unit 0 / 1, lane l
+        // the x rows 4l .. 4l+3 of this CTA's half of the tile (one gather4 per unit)
+        const int half = t.ncols / 2;
+        const uint32_t tok_bytes = (uint32_t)half * KU * 2;
+        for (int kb = 0; kb < t.kb; ++kb) {
+          const int nu = min(UNITS, t.ku - kb * UNITS);
+          const int uw = lane & 1;
+          const Boxes b = boxes_of<MODE>(p, t, t.ku0 + kb * UNITS + uw, rank);
+          const int kx = (t.ku0 + kb * UNITS) * KU;
+          const uint32_t fb = mapa_shared(bar(c.full[stage]), 0);
+          const uint32_t sa = sbase + stage * STAGE_BYTES + uw * A_UNIT;
+          const uint32_t sg = sbase + stage * STAGE_BYTES + A_BYTES + lane * (4 * KU * 2);
+          const uint32_t tx = 2 * nu * (A_UNIT + tok_bytes);
+          if (!warp_wait_bounded(bar(c.empty[stage]), phase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[stage]), tx);
+          __syncwarp();
+          if (lane < nu) tma_load_5d_pair(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1);
+          if (4 * lane < half) {
+            tma_gather4_pair(sg, &p.tmXg, fb, kx, rows.x, rows.y, rows.z, rows.w);
+            if (nu > 1)
+              tma_gather4_pair(sg + B_UNIT, &p.tmXg, fb, kx + KU, rows.x, rows.y, rows.z, rows.w);
+          }
+          __syncwarp();
+          issued_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        continue;
+      }
       for (int kb = 0; kb < t.kb; ++kb) {
         // everything the stage's copies need is computed before waiting for the slot
         const int nu = min(UNITS, t.ku - kb * UNITS);             // units in this block
@@ -607,14 +677,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     int cur = pair;
     for (;;) {
       Tile t;
+      const TcParams* gp = (MODE == MODE_UP && p.row_token != nullptr) ? &p : nullptr;
       if (rank == 0) {
         t = cur < total ? decode_tile<MODE>(p, c, cur) : end_tile();
-        if (!ring_publish(c, qs, qph, t, abort_flag, p.err) ||
+        if (!ring_publish(c, qs, qph, t, abort_flag, p.err, gp, rank) ||
             !ring_send(c, qs, qph, t, abort_flag, p.err))
           break;
       } else {
         if (!ring_recv(c, qs, qph, t, abort_flag, p.err) ||
-            !ring_publish(c, qs, qph, t, abort_flag, p.err))
+            !ring_publish(c, qs, qph, t, abort_flag, p.err, gp, rank))
           break;
       }
       if (++qs == SQ) { qs = 0; qph ^= 1u; }
@@ -709,6 +780,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 // u[t, e] = gate_bias[e] + sum over splits s (in order) of part[s, t, e].
 __global__ void __launch_bounds__(256) gate_reduce_kernel(const float* part, int splits, int T,
                                                           int N, const float* bias, float* u) {
+  pdl_wait();
+  pdl_trigger();
   const size_t n = (size_t)T * N;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -721,6 +794,8 @@ __global__ void __launch_bounds__(256) gate_reduce_kernel(const float* part, int
 // One CTA waits on an mbarrier that nothing ever arrives on; the bounded wait must give up,
 // raise the error word and return.
 __global__ void wait_selftest_kernel(int* err, unsigned long long timeout_ns) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint64_t b;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -788,16 +863,18 @@ cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
   int grid = (dev >= 0 && dev < 64) ? grid_for_device[dev] : 0;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (grid == 0) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -859,14 +936,20 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
     if (e != cudaSuccess || prm.splits == 1) return e;
     int blocks = (int)(((size_t)T * N + 255) / 256);
     if (blocks > num_sms * 8) blocks = num_sms * 8;
-    gate_reduce_kernel<<<blocks, 256, 0, st>>>(a.gate_part, prm.splits, (int)T, (int)N, a.gate_bias,
-                                               static_cast<float*>(a.out0));
-    note_launches(1);
-    return cudaGetLastError();
+    return launch_pdl(gate_reduce_kernel, dim3(blocks), dim3(256), 0, st,
+                      static_cast<const float*>(a.gate_part), prm.splits, (int)T, (int)N,
+                      a.gate_bias, static_cast<float*>(a.out0));
   }
   if (a.mode == MODE_UP) {
-    if (a.n_routed > 0) ok = ok && make_up_weight_map(&prm.tmW0, a.b0, H, I, N) &&
-                             make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, R);
+    if (a.n_routed > 0) {
+      ok = ok && make_up_weight_map(&prm.tmW0, a.b0, H, I, N);
+      if (a.row_token != nullptr) {
+        ok = ok && make_map(&prm.tmXg, a.a0, H, T, 1);  // x [T, H], rows gathered
+        prm.row_token = a.row_token;
+      } else {
+        ok = ok && make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, R);
+      }
+    }
     if (a.has_shared) ok = ok && make_up_weight_map(&prm.tmW1, a.b1, H, I, S) &&
                            make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, H, T);
     if (!ok) return cudaErrorInvalidValue;
@@ -881,9 +964,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
 }
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long timeout_ns, cudaStream_t st) {
-  wait_selftest_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, st, err, timeout_ns);
 }
 
 }  // namespace moe

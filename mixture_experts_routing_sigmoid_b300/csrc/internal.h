@@ -10,6 +10,26 @@ namespace moe {
 // Count of kernels this library has launched (abi.cu); every launcher adds its launches.
 void note_launches(int n);
 
+// Launch with programmatic stream serialization: the kernel's CTAs may start (and run their
+// prologue) while the kernel ahead of it in the stream is finishing; each kernel of this library
+// waits for its predecessor (pdl_wait) before its first access to global memory. Counts the launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  note_launches(1);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- routing (route.cu)
 struct RouteArgs {
   int T, N, K, G, Gk, topn, score_fn, norm_topk, precise_w;
@@ -87,6 +107,8 @@ struct PermuteArgs {
   int32_t* cnt;         // [nb, N]
   int32_t* base;        // [nb, N]
   unsigned long long* thr;  // [D]
+  int32_t* sched_zero;  // nullptr, or two tile counters the permutation sets to zero (the expert
+                        // GEMMs that follow claim tiles from them)
   int* err;
 };
 int permute_blocks(int T);
@@ -128,6 +150,8 @@ struct GemmArgs {
   size_t gate_part_floats;  // capacity of gate_part
   int* sched;               // UP / DOWN (tcgen05): tile counter, zero at launch, for the dynamic
                             // tile schedule; nullptr: static round-robin schedule
+  const int32_t* row_token; // UP (tcgen05) row gather: routed row r is x[row_token[r]], with
+                            // a0 = x [T,H]; nullptr: a0 = x_perm
   int* err;
 };
 // Rows (of N floats) of the gate GEMM's split-K scratch the workspace provides.

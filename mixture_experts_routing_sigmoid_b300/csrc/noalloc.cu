@@ -102,6 +102,7 @@ extern "C" moe_status moe_permute_static_scratch(const moe_config* cfg, int32_t 
   p.cnt = reinterpret_cast<int32_t*>(base + kMaskBytes);
   p.base = reinterpret_cast<int32_t*>(base + kMaskBytes + kCountBytes);
   p.thr = reinterpret_cast<unsigned long long*>(base + kMaskBytes + 2 * kCountBytes);
+  p.sched_zero = nullptr;
   p.err = moe::abi_error_word();
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   st = moe::abi_cuda_status(moe::launch_permute(p, moe::abi_num_sms(), cs),

@@ -29,6 +29,8 @@ __device__ __forceinline__ unsigned long long drop_key(float w, long long a) {
 }
 
 __global__ void __launch_bounds__(1024) drop_threshold_kernel(PermuteArgs p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned int hist[256];
   __shared__ unsigned long long s_prefix;
   __shared__ long long s_remaining;
@@ -85,6 +87,8 @@ __device__ __forceinline__ bool is_kept(const PermuteArgs& p, long long a, int e
 }
 
 __global__ void __launch_bounds__(PB) perm_hist_kernel(PermuteArgs p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t sm[];  // [N][8]
   for (int i = threadIdx.x; i < p.N * 8; i += PB) sm[i] = 0;
   __syncthreads();
@@ -109,6 +113,8 @@ __global__ void __launch_bounds__(PB) perm_hist_kernel(PermuteArgs p) {
 }
 
 __global__ void __launch_bounds__(256) perm_scan_kernel(PermuteArgs p, int nb) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int tot[256];
   __shared__ int excl[257];
   const int e = threadIdx.x;
@@ -133,10 +139,15 @@ __global__ void __launch_bounds__(256) perm_scan_kernel(PermuteArgs p, int nb) {
     p.offsets[e] = off;
     for (int b = 0; b < nb; ++b) p.base[(size_t)b * p.N + e] += off;
   }
-  if (e == 0) p.offsets[p.N] = excl[p.N];
+  if (e == 0) {
+    p.offsets[p.N] = excl[p.N];
+    if (p.sched_zero != nullptr) { p.sched_zero[0] = 0; p.sched_zero[1] = 0; }
+  }
 }
 
 __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * PB + threadIdx.x;
   if (t >= p.T) return;
   const int wi = threadIdx.x >> 5;
@@ -160,6 +171,8 @@ __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
 // bitmasks ([N][W] words, W = ceil(T / 32)) in shared memory.
 constexpr int SB_MAX_T = 1024;
 __global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t sm[];  // [N][W] masks, then [N + 1] exclusive offsets
   const int W = (p.T + 31) >> 5;
   int* excl = reinterpret_cast<int*>(sm + p.N * W);
@@ -200,6 +213,7 @@ __global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs
       excl[p.N] = before + incl;
       p.offsets[p.N] = before + incl;
     }
+    if (e == 0 && p.sched_zero != nullptr) { p.sched_zero[0] = 0; p.sched_zero[1] = 0; }
   }
   __syncthreads();
   if (t < p.T) {
@@ -224,6 +238,8 @@ __global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs
 // the token. Consecutive threads take consecutive chunks of a row, so every warp reads and
 // writes contiguous runs; a batch of a few tokens still spreads over the whole GPU.
 __global__ void __launch_bounds__(256) dispatch_rows_kernel(PermuteArgs p) {
+  pdl_wait();
+  pdl_trigger();
   const size_t row_bytes = (size_t)p.H * p.elem_bytes;
   const int chunks = (int)(row_bytes / 16);
   const size_t n = (size_t)p.T * chunks;
@@ -253,22 +269,20 @@ cudaError_t launch_permute(const PermuteArgs& p, int num_sms, cudaStream_t st) {
   }
   const int nb = permute_blocks(p.T);
   if (p.capacity_drop) {
-    drop_threshold_kernel<<<p.D, 1024, 0, st>>>(p);
-    note_launches(1);
+    const cudaError_t e = launch_pdl(drop_threshold_kernel, dim3(p.D), dim3(1024), 0, st, p);
+    if (e != cudaSuccess) return e;
   }
   if (p.T <= SB_MAX_T) {
     const int W = (p.T + 31) / 32;
     int threads = ((p.T + 31) / 32) * 32;
     if (threads < p.N) threads = ((p.N + 31) / 32) * 32;
-    perm_single_block_kernel<<<1, threads, (p.N * W + p.N + 1) * sizeof(uint32_t), st>>>(p);
-    note_launches(1);
-    return cudaGetLastError();
+    return launch_pdl(perm_single_block_kernel, dim3(1), dim3(threads),
+                      (p.N * W + p.N + 1) * sizeof(uint32_t), st, p);
   }
-  perm_hist_kernel<<<nb, PB, p.N * 8 * sizeof(uint32_t), st>>>(p);
-  perm_scan_kernel<<<1, 256, 0, st>>>(p, nb);
-  perm_scatter_kernel<<<nb, PB, 0, st>>>(p);
-  note_launches(3);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(perm_hist_kernel, dim3(nb), dim3(PB), p.N * 8 * sizeof(uint32_t), st, p);
+  if (e == cudaSuccess) e = launch_pdl(perm_scan_kernel, dim3(1), dim3(256), 0, st, p, nb);
+  if (e == cudaSuccess) e = launch_pdl(perm_scatter_kernel, dim3(nb), dim3(PB), 0, st, p);
+  return e;
 }
 
 cudaError_t launch_dispatch(const PermuteArgs& p, int num_sms, cudaStream_t st) {
@@ -276,9 +290,7 @@ cudaError_t launch_dispatch(const PermuteArgs& p, int num_sms, cudaStream_t st) 
   const size_t n = (size_t)p.T * ((size_t)p.H * p.elem_bytes / 16);
   size_t blocks = (n + 255) / 256;
   if (blocks > (size_t)num_sms * 16) blocks = (size_t)num_sms * 16;
-  dispatch_rows_kernel<<<(int)blocks, 256, 0, st>>>(p);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_rows_kernel, dim3((int)blocks), dim3(256), 0, st, p);
 }
 
 }  // namespace moe

@@ -6,14 +6,24 @@
 //   key_e = s_e + b_e, s = softmax(u) or sigmoid(u);
 //   group score = sum of the group's top-n keys; keep the best Gk groups (ties: lower group);
 //   take the K best keys among their experts (ties: lower expert); w = s (/sum) * scale.
+// The order is that of the real numbers key_e (and of the real sums of them). Two values closer
+// than 2^-80 of their size count as equal, and the lower index wins, as for exact ties.
 //
-// One warp routes one token; lane l holds experts l, l+32, ... (coalesced loads of the
-// logit row). Keys are first evaluated in fp32. The chosen set then equals the exact (fp64)
-// one unless a decision margin (K-th vs (K+1)-th eligible key, Gk-th vs (Gk+1)-th group
-// score) lies within the fp32 error bound of the keys; such a token is rechecked by the same
-// warp: for a sigmoid gate only the groups and experts inside the error band are rescored in
-// fp64 (refine_sigmoid), otherwise the whole token is redone in fp64. For a softmax gate with no selection bias and max-based (or no) group scores the
-// logits themselves order the experts exactly (softmax is monotone), so no exp is needed.
+// One warp routes one token; lane l holds experts l, l+32, ... (coalesced loads of the logit
+// row). Keys are first evaluated in fp32 and the choice is made with warp reductions
+// (redux.sync max / min over order-preserving integer images of the keys: one reduction per
+// group score half, per kept group and per chosen expert). That choice is the real one unless a
+// decision margin (K-th vs (K+1)-th eligible key, Gk-th vs (Gk+1)-th group score) lies within the
+// fp32 error bound of the keys. Such a token is rechecked by the same warp:
+//   - sigmoid gate: only the groups and experts inside the error band are rescored, in
+//     double-double arithmetic (~100 bits, refine_sigmoid), which settles their real order;
+//   - softmax gate with no selection bias and max-based (or no) group scores: the logits
+//     themselves give the real order (softmax is monotone), so nothing is ever rechecked;
+//   - other softmax combinations (a selection bias, or group scores that sum two keys; no page
+//     describes them): the token is redone with fp64 keys, whose order matches the real one
+//     except for keys within a few fp64 units of each other.
+// Weights are fp32 (within a few ulps), or, when the v2 drop will rank them, computed in fp64
+// and rounded once.
 #include "common.cuh"
 #include "internal.h"
 
@@ -51,13 +61,121 @@ __device__ __forceinline__ KT warp_max(KT v) {
   return v;
 }
 
+// Order-preserving map of a non-NaN float onto uint32 (0 stays free: "no key").
+__device__ __forceinline__ uint32_t ord32(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unord32(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+__device__ __forceinline__ float key_tol(float v) {
+  // Bound on |fp32 key - real key|: a sigmoid or softmax score carries a few ulps of error
+  // (expf <= 2 ulp, one IEEE division, one sum), the + bias one rounding; 2e-6 * max(1,|v|)
+  // is several times that bound.
+  return 2e-6f * fmaxf(1.0f, fabsf(v));
+}
+
+// ---------------------------------------------------------------- fp32 choice (redux)
+struct FastSel {
+  int e;          // lane r < K: the r-th chosen expert (in choice order)
+  float se;       // lane r < K: its score s
+  float ssum;     // sum of the K chosen scores (every lane)
+  float kth;      // K-th chosen key
+  float next;     // best remaining eligible key (-inf if none)
+  float gkth;     // Gk-th group score (+inf if G == Gk)
+  float gnext;    // (Gk+1)-th group score (-inf if none)
+  uint32_t gmask; // kept groups
+  bool ok;
+};
+
+// gj[j]: group of this lane's expert j*32 + lane; ok[j]: its ordered key (0: no expert).
+__device__ __forceinline__ FastSel fast_select(const uint32_t (&ok)[MAXJ], const float (&s)[MAXJ],
+                                               const int (&gj)[MAXJ], int lane, int K, int G,
+                                               int Gk, int topn) {
+  FastSel out;
+  out.ok = true;
+  out.gmask = 0xffffffffu;
+  out.gkth = INFINITY;
+  out.gnext = -INFINITY;
+  if (G > Gk) {
+    // group scores: the group's best key, plus (topn == 2) the best of the rest
+    float gs = -INFINITY;  // lane g < G: group g's score
+    for (int g = 0; g < G; ++g) {
+      uint32_t l1 = 0, l2 = 0;
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        if (gj[j] == g) {
+          const uint32_t v = ok[j];
+          if (v > l1) { l2 = l1; l1 = v; } else if (v > l2) { l2 = v; }
+        }
+      }
+      const uint32_t m1 = __reduce_max_sync(FULL_MASK, l1);
+      float v = unord32(m1);
+      if (topn == 2) {
+        const int holder = __ffs(__ballot_sync(FULL_MASK, l1 == m1)) - 1;
+        v += unord32(__reduce_max_sync(FULL_MASK, lane == holder ? l2 : l1));
+      }
+      if (lane == g) gs = v;
+    }
+    const uint32_t go = lane < G ? ord32(gs) : 0u;
+    bool taken = false;
+    uint32_t last = 0;
+    out.gmask = 0;
+    for (int r = 0; r <= Gk && r < G; ++r) {
+      const uint32_t v = taken ? 0u : go;
+      const uint32_t m = __reduce_max_sync(FULL_MASK, v);
+      const uint32_t bal = __ballot_sync(FULL_MASK, m != 0u && v == m);
+      if (bal == 0u) { out.ok = false; break; }
+      const int gi = __ffs(bal) - 1;  // the lowest group among equal scores
+      if (r < Gk) {
+        out.gmask |= 1u << gi;
+        if (lane == gi) taken = true;
+        last = m;
+      } else {
+        out.gnext = unord32(m);
+      }
+    }
+    out.gkth = last ? unord32(last) : -INFINITY;
+  }
+  uint32_t avail = 0;  // bit j: expert j*32 + lane is eligible and not chosen yet
+#pragma unroll
+  for (int j = 0; j < MAXJ; ++j)
+    if (ok[j] != 0u && gj[j] >= 0 && ((out.gmask >> gj[j]) & 1u)) avail |= 1u << j;
+  out.e = -1;
+  out.se = 0.0f;
+  out.ssum = 0.0f;
+  out.next = -INFINITY;
+  uint32_t kth = 0;
+  for (int r = 0; r <= K; ++r) {
+    uint32_t best = 0;
+    int bj = 0;
+    float bs = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j)
+      if (((avail >> j) & 1u) && ok[j] > best) { best = ok[j]; bj = j; bs = s[j]; }
+    const uint32_t m = __reduce_max_sync(FULL_MASK, best);
+    if (r == K) {
+      if (m != 0u) out.next = unord32(m);
+      break;
+    }
+    if (m == 0u) { out.ok = false; break; }
+    // the lowest expert among the lanes holding the maximum (each lane offers its lowest)
+    const uint32_t e = __reduce_min_sync(FULL_MASK, best == m ? (uint32_t)(bj * 32 + lane) : ~0u);
+    const float se = __shfl_sync(FULL_MASK, bs, e & 31);
+    if (lane == (int)(e & 31)) avail &= ~(1u << (e >> 5));
+    if (lane == r) { out.e = (int)e; out.se = se; }
+    out.ssum += se;
+    kth = m;
+  }
+  out.kth = kth ? unord32(kth) : -INFINITY;
+  return out;
+}
+
+// ---------------------------------------------------------------- fp64 choice (cold path)
 struct Selection {
   int e;           // lane r < K: the r-th chosen expert
-  double kth;      // key of the K-th choice
-  double emargin;  // K-th key minus best remaining eligible key (+inf if none)
-  double gkth;     // Gk-th group score
-  double gmargin;  // Gk-th minus (Gk+1)-th group score (+inf if G == Gk)
-  uint32_t gmask;  // chosen groups
   bool ok;
 };
 
@@ -68,52 +186,26 @@ __device__ __forceinline__ KT group_scores(const KT (&key)[MAXJ], int lane, int 
                                            int J) {
   const int gsz = N / G;
   KT my_gs = neg_inf<KT>();
-  {
-    if (gsz == 32 && G == J) {
-      // group g is register g of every lane: reduce all groups' top-2 side by side
-      KT a1[MAXJ], a2[MAXJ];
+  for (int g = 0; g < G; ++g) {
+    KT a1 = neg_inf<KT>(), a2 = neg_inf<KT>();
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j) {
-        a1[j] = j < J ? key[j] : neg_inf<KT>();
-        a2[j] = neg_inf<KT>();
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j) {
-          const KT b1 = __shfl_xor_sync(FULL_MASK, a1[j], o);
-          const KT b2 = __shfl_xor_sync(FULL_MASK, a2[j], o);
-          const KT n2 = max(min(a1[j], b1), max(a2[j], b2));
-          a1[j] = max(a1[j], b1);
-          a2[j] = n2;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < MAXJ; ++j)
-        if (lane == j) my_gs = (topn == 1) ? a1[j] : a1[j] + a2[j];
-    } else {
-      for (int g = 0; g < G; ++g) {
-        KT a1 = neg_inf<KT>(), a2 = neg_inf<KT>();
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j) {
-          const int e = j * 32 + lane;
-          if (j < J && e < N && e / gsz == g) {
-            const KT v = key[j];
-            if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const KT b1 = __shfl_xor_sync(FULL_MASK, a1, o);
-          const KT b2 = __shfl_xor_sync(FULL_MASK, a2, o);
-          const KT n1 = max(a1, b1);
-          const KT n2 = max(min(a1, b1), max(a2, b2));
-          a1 = n1; a2 = n2;
-        }
-        const KT gsv = (topn == 1) ? a1 : a1 + a2;
-        if (lane == g) my_gs = gsv;
+    for (int j = 0; j < MAXJ; ++j) {
+      const int e = j * 32 + lane;
+      if (j < J && e < N && e / gsz == g) {
+        const KT v = key[j];
+        if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const KT b1 = __shfl_xor_sync(FULL_MASK, a1, o);
+      const KT b2 = __shfl_xor_sync(FULL_MASK, a2, o);
+      const KT n1 = max(a1, b1);
+      const KT n2 = max(min(a1, b1), max(a2, b2));
+      a1 = n1; a2 = n2;
+    }
+    const KT gsv = (topn == 1) ? a1 : a1 + a2;
+    if (lane == g) my_gs = gsv;
   }
   return my_gs;
 }
@@ -126,30 +218,19 @@ __device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int l
   out.ok = true;
   const int gsz = N / G;
   uint32_t gmask = 0xffffffffu;
-  out.gmargin = INFINITY;
-  out.gkth = INFINITY;
   if (G > 1) {
     const KT my_gs = group_scores<KT>(key, lane, N, G, topn, J);
     gmask = 0;
     bool taken = false;
-    KT last = neg_inf<KT>();
-    for (int r = 0; r <= Gk && r < G; ++r) {
+    for (int r = 0; r < Gk && r < G; ++r) {
       KT v = (lane < G && !taken) ? my_gs : neg_inf<KT>();
       int i = (lane < G && !taken) ? lane : 0x7fffffff;
       warp_argmax(v, i);
-      if (r < Gk) {
-        if (i == 0x7fffffff) { out.ok = false; break; }
-        gmask |= 1u << i;
-        if (lane == i) taken = true;
-        last = v;
-      } else {
-        out.gmargin = (double)last - (double)v;
-      }
+      if (i == 0x7fffffff) { out.ok = false; break; }
+      gmask |= 1u << i;
+      if (lane == i) taken = true;
     }
-    out.gkth = (double)last;
   }
-  out.gmask = gmask;
-
   uint32_t elig = 0, taken = 0;
 #pragma unroll
   for (int j = 0; j < MAXJ; ++j) {
@@ -157,8 +238,7 @@ __device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int l
     if (j < J && e < N && ((gmask >> (e / gsz)) & 1u)) elig |= 1u << j;
   }
   out.e = -1;
-  KT kth = neg_inf<KT>();
-  for (int r = 0; r <= K; ++r) {
+  for (int r = 0; r < K; ++r) {
     KT v = neg_inf<KT>();
     int i = 0x7fffffff;
 #pragma unroll
@@ -168,69 +248,129 @@ __device__ __forceinline__ Selection select_experts(const KT (&key)[MAXJ], int l
       }
     }
     warp_argmax(v, i);
-    if (r < K) {
-      if (i == 0x7fffffff) { out.ok = false; break; }
+    if (i == 0x7fffffff) { out.ok = false; break; }
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j)
-        if (i == j * 32 + lane) taken |= 1u << j;
-      if (lane == r) out.e = i;
-      kth = v;
-    } else {
-      out.emargin = (i == 0x7fffffff) ? (double)INFINITY : (double)kth - (double)v;
-    }
+    for (int j = 0; j < MAXJ; ++j)
+      if (i == j * 32 + lane) taken |= 1u << j;
+    if (lane == r) out.e = i;
   }
-  out.kth = (double)kth;
   return out;
 }
 
-__device__ __forceinline__ float key_tol(double v) {
-  // Bound on |fp32 key - exact key|: a sigmoid or softmax score carries a few ulps of error
-  // (expf <= 2 ulp, one IEEE division, one sum), the + bias one rounding; 2e-6 * max(1,|v|)
-  // is several times that bound.
-  return 2e-6f * fmaxf(1.0f, fabsf((float)v));
+// ---------------------------------------------------------------- double-double arithmetic
+// Values as unevaluated sums hi + lo of two doubles (~106 bits), from the error-free
+// transformations of Knuth (two-sum) and Dekker (two-product, here with an FMA). The exp follows
+// the scheme of Hida, Li and Bailey's double-double library: reduce by k ln 2, scale by 2^-9, a
+// Taylor series for expm1, nine doublings expm1(2y) = 2 expm1(y) + expm1(y)^2, then 2^k.
+struct DD {
+  double hi, lo;
+};
+__device__ __forceinline__ DD dd_two_sum(double a, double b) {
+  const double s = a + b;
+  const double bb = s - a;
+  return {s, (a - (s - bb)) + (b - bb)};
 }
-
-// One out-of-line copy: the recheck runs for a handful of tokens per launch, with its code
-// fetched cold, so its size (not its arithmetic) sets its cost.
-__device__ __noinline__ double exact_sigmoid_key(float u, float b) {
-  return 1.0 / (1.0 + exp(-(double)u)) + (double)b;
+__device__ __forceinline__ DD dd_fast_two_sum(double a, double b) {  // |a| >= |b|
+  const double s = a + b;
+  return {s, b - (s - a)};
 }
-
-// Order-preserving map of a (non-NaN) double onto a signed 64-bit integer: comparisons of the
-// exact keys run on the integer pipes instead of the (slow) fp64 one.
-__device__ __forceinline__ long long ord64(double d) {
-  const long long i = __double_as_longlong(d);
-  return i >= 0 ? i : i ^ 0x7fffffffffffffffll;
+__device__ __forceinline__ DD dd_add(DD a, DD b) {
+  DD s = dd_two_sum(a.hi, b.hi);
+  const DD t = dd_two_sum(a.lo, b.lo);
+  s.lo += t.hi;
+  s = dd_fast_two_sum(s.hi, s.lo);
+  s.lo += t.lo;
+  return dd_fast_two_sum(s.hi, s.lo);
 }
-constexpr long long ORD_NONE = (long long)0x8000000000000000ull;  // below every ord64
-__device__ __forceinline__ double unord64(long long o) {
-  return __longlong_as_double(o >= 0 ? o : o ^ 0x7fffffffffffffffll);
+__device__ __forceinline__ DD dd_neg(DD a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ DD dd_mul(DD a, DD b) {
+  const double p = a.hi * b.hi;
+  double e = fma(a.hi, b.hi, -p);
+  e = fma(a.hi, b.lo, e);
+  e = fma(a.lo, b.hi, e);
+  return dd_fast_two_sum(p, e);
 }
-
-// Warp-wide argmax on (ordered key desc, index asc); result in every lane.
-__device__ __forceinline__ void warp_argmax_ord(long long& v, int& i) {
+__device__ __forceinline__ DD dd_mul_d(DD a, double b) {
+  const double p = a.hi * b;
+  double e = fma(a.hi, b, -p);
+  e = fma(a.lo, b, e);
+  return dd_fast_two_sum(p, e);
+}
+__device__ __forceinline__ DD dd_div(DD a, DD b) {
+  const double q1 = a.hi / b.hi;
+  DD r = dd_add(a, dd_neg(dd_mul_d(b, q1)));
+  const double q2 = r.hi / b.hi;
+  r = dd_add(r, dd_neg(dd_mul_d(b, q2)));
+  const double q3 = r.hi / b.hi;
+  return dd_add(dd_fast_two_sum(q1, q2), DD{q3, 0.0});
+}
+__device__ __noinline__ DD dd_exp(double x) {
+  if (x > 709.0) return {INFINITY, 0.0};
+  if (x < -745.0) return {0.0, 0.0};
+  const DD ln2 = {0x1.62e42fefa39efp-1, 0x1.abc9e3b39803fp-56};
+  const double k = rint(x / ln2.hi);
+  DD r = dd_add(DD{x, 0.0}, dd_neg(dd_mul_d(ln2, k)));
+  r.hi *= 0x1p-9;
+  r.lo *= 0x1p-9;
+  DD p = r, s = r;
+#pragma unroll 1
+  for (int n = 2; n <= 10; ++n) {
+    p = dd_div(dd_mul(p, r), DD{(double)n, 0.0});
+    s = dd_add(s, p);
+  }
+#pragma unroll 1
+  for (int i = 0; i < 9; ++i) s = dd_add(dd_mul_d(s, 2.0), dd_mul(s, s));
+  s = dd_add(s, DD{1.0, 0.0});
+  const int ki = (int)k;
+  return {ldexp(s.hi, ki), ldexp(s.lo, ki)};
+}
+// sigmoid(u) + b in double-double.
+__device__ __noinline__ DD dd_sigmoid_key(float u, float b) {
+  const DD e = dd_exp(-(double)u);
+  DD s = {0.0, 0.0};
+  if (e.hi != INFINITY) s = dd_div(DD{1.0, 0.0}, dd_add(DD{1.0, 0.0}, e));
+  return dd_add(s, DD{(double)b, 0.0});
+}
+// Real order with ties: -1 if a is larger, +1 if b is, 0 if they are within 2^-80 of their size.
+__device__ __forceinline__ int dd_cmp(DD a, DD b) {
+  const DD d = dd_add(a, dd_neg(b));
+  const double tie = 0x1p-80 * fmax(fabs(a.hi), fabs(b.hi));
+  return d.hi > tie ? -1 : (d.hi < -tie ? 1 : 0);
+}
+// Warp-wide argmax of (dd value desc under dd_cmp, index asc) over lanes with `valid`; i = -1 if
+// no lane is valid. Result in every lane.
+__device__ __forceinline__ void warp_argmax_dd(DD& v, int& i, bool valid) {
+  if (!valid) i = -1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const long long ov = __shfl_xor_sync(FULL_MASK, v, o);
+    DD ov;
+    ov.hi = __shfl_xor_sync(FULL_MASK, v.hi, o);
+    ov.lo = __shfl_xor_sync(FULL_MASK, v.lo, o);
     const int oi = __shfl_xor_sync(FULL_MASK, i, o);
-    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+    bool take;
+    if (oi < 0) take = false;
+    else if (i < 0) take = true;
+    else {
+      const int c = dd_cmp(ov, v);
+      take = c < 0 || (c == 0 && oi < i);
+    }
+    if (take) { v = ov; i = oi; }
   }
 }
 
-// Exact selection for a sigmoid gate whose fp32 decision lies within its error bound. Every
-// fp32 key is within tol of its exact (fp64) value and every fp32 group score within gtol, so a
-// group whose fp32 score exceeds the Gk-th by more than 2 gtol is among the exact best Gk, one
-// below it by more than 2 gtol is not, and only the groups inside that band are rescored in
-// fp64 (all their experts) when the band holds more groups than places left; likewise for the
-// experts around the K-th eligible key with 2 tol. The band's members are ranked by their exact
-// values (ties: lower index). The keys are recomputed here from the logits exactly as the fp32
-// pass computes them. Lane r < K receives the r-th chosen expert in ascending order; false if a
-// rank is missing (the caller then redoes the token entirely in fp64). fp_gmask and fp_kth are
-// the fp32 pass's chosen groups and K-th key: when the groups stand, its K-th key is reused.
+// Exact selection for a sigmoid gate whose fp32 decision lies within its error bound. Every fp32
+// key is within tol of its real value and every fp32 group score within gtol, so a group whose
+// fp32 score exceeds the Gk-th by more than 2 gtol is among the real best Gk, one below it by more
+// than 2 gtol is not, and only the groups inside that band are rescored in double-double (all
+// their experts) when the band holds more groups than places left; likewise for the experts
+// around the K-th eligible key with 2 tol. The band's members are ranked by their real values
+// (dd_cmp; ties: lower index). The fp32 keys are recomputed here from the logits exactly as the
+// fp32 pass computes them. Lane r < K receives the r-th chosen expert; false if a rank is missing.
+// fp_gmask and fp_kth are the fp32 pass's chosen groups and K-th key: when the groups stand, its
+// K-th key is reused.
 __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, int lane, int N,
                                             int K, int G, int Gk, int topn, uint32_t fp_gmask,
                                             float fp_kth, int& sel_e) {
-  constexpr int NONE = 0x7fffffff;
   const int J = (N + 31) >> 5;
   const int gsz = N / G;
   float u[MAXJ], b[MAXJ], key[MAXJ];
@@ -257,7 +397,7 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
     }
     const uint32_t at = __ballot_sync(FULL_MASK, lane < G && rnk == Gk - 1);
     const double vg = (double)__shfl_sync(FULL_MASK, gs, __ffs(at) - 1);
-    const double gtol = topn * (double)key_tol(kmax) + 6e-8 * fabs(vg);
+    const double gtol = topn * (double)key_tol((float)kmax) + 6e-8 * fabs(vg);
     const bool in = lane < G && (double)gs > vg + 2.0 * gtol;
     const uint32_t cin = __ballot_sync(FULL_MASK, in);
     const uint32_t band = __ballot_sync(FULL_MASK, lane < G && !in && (double)gs >= vg - 2.0 * gtol);
@@ -266,38 +406,53 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
     if (__popc(band) == need) {
       picked = band;  // every band group is in: no exact score needed
     } else {
-      long long gx = ORD_NONE;  // lane g: exact score of band group g (ordered)
+      DD gx = {0.0, 0.0};  // lane g: real score of band group g
       for (uint32_t m = band; m; m &= m - 1) {
         const int g = __ffs(m) - 1;
-        long long a1 = ORD_NONE, a2 = ORD_NONE;
-        if (gsz == 32 && G == J) {  // group g is register g of every lane
-          a1 = ord64(exact_sigmoid_key(u[g], b[g]));
-        } else {
+        // the group's top-n real keys: lane-local top-2, then a warp top-2
+        DD a1 = {0.0, 0.0}, a2 = {0.0, 0.0};
+        bool h1 = false, h2 = false;
 #pragma unroll 1
-          for (int j = 0; j < MAXJ; ++j) {
-            const int e = j * 32 + lane;
-            const bool mine = j < J && e < N && e / gsz == g;
-            if (__any_sync(FULL_MASK, mine) && mine) {
-              const long long o = ord64(exact_sigmoid_key(u[j], b[j]));
-              if (o > a1) { a2 = a1; a1 = o; } else if (o > a2) { a2 = o; }
-            }
+        for (int j = 0; j < MAXJ; ++j) {
+          const int e = j * 32 + lane;
+          const bool mine = j < J && e < N && e / gsz == g;
+          if (__any_sync(FULL_MASK, mine) && mine) {
+            const DD k = dd_sigmoid_key(u[j], b[j]);
+            if (!h1 || dd_cmp(k, a1) < 0) { a2 = a1; h2 = h1; a1 = k; h1 = true; }
+            else if (!h2 || dd_cmp(k, a2) < 0) { a2 = k; h2 = true; }
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {  // top-2 of the group, compared as integers
-          const long long b1 = __shfl_xor_sync(FULL_MASK, a1, o);
-          const long long b2 = __shfl_xor_sync(FULL_MASK, a2, o);
-          if (b1 > a1) { a2 = max(a1, b2); a1 = b1; }
-          else { a2 = max(a2, b1); }
+#pragma unroll 1
+        for (int o = 16; o > 0; o >>= 1) {
+          DD b1, b2;
+          b1.hi = __shfl_xor_sync(FULL_MASK, a1.hi, o);
+          b1.lo = __shfl_xor_sync(FULL_MASK, a1.lo, o);
+          b2.hi = __shfl_xor_sync(FULL_MASK, a2.hi, o);
+          b2.lo = __shfl_xor_sync(FULL_MASK, a2.lo, o);
+          const bool g1 = __shfl_xor_sync(FULL_MASK, h1, o);
+          const bool g2 = __shfl_xor_sync(FULL_MASK, h2, o);
+          // merge the two sorted pairs (a1 >= a2, b1 >= b2) into the top two
+          if (g1 && (!h1 || dd_cmp(b1, a1) < 0)) {
+            // b1 is the largest; the second is the larger of a1 and b2
+            const bool second_b2 = g2 && (!h1 || dd_cmp(b2, a1) < 0);
+            a2 = second_b2 ? b2 : a1;
+            h2 = second_b2 ? true : h1;
+            a1 = b1;
+            h1 = true;
+          } else if (g1 && (!h2 || dd_cmp(b1, a2) < 0)) {
+            a2 = b1;
+            h2 = true;
+          }
         }
-        if (lane == g) gx = ord64(topn == 1 ? unord64(a1) : unord64(a1) + unord64(a2));
+        const DD score = (topn == 1 || !h2) ? a1 : dd_add(a1, a2);
+        if (lane == g) gx = score;
       }
       for (int r = 0; r < need; ++r) {
         const bool cand = ((band & ~picked) >> lane) & 1u;
-        long long v = cand ? gx : ORD_NONE;
-        int i = cand ? lane : NONE;
-        warp_argmax_ord(v, i);
-        if (i == NONE) return false;
+        DD v = gx;
+        int i = lane;
+        warp_argmax_dd(v, i, cand);
+        if (i < 0) return false;
         picked |= 1u << i;
       }
     }
@@ -314,13 +469,13 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
   uint32_t taken = 0;
   for (int r = 0; r < K && gmask != fp_gmask; ++r) {
     float v = -INFINITY;
-    int i = NONE;
+    int i = 0x7fffffff;
 #pragma unroll 1
     for (int j = 0; j < MAXJ; ++j)
       if (((elig & ~taken) >> j) & 1u)
-        if (key[j] > v || i == NONE) { v = key[j]; i = j * 32 + lane; }
+        if (key[j] > v || i == 0x7fffffff) { v = key[j]; i = j * 32 + lane; }
     warp_argmax(v, i);
-    if (i == NONE) return false;
+    if (i == 0x7fffffff) return false;
 #pragma unroll 1
     for (int j = 0; j < MAXJ; ++j)
       if (i == j * 32 + lane) taken |= 1u << j;
@@ -341,22 +496,23 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
   if (warp_sum(__popc(band)) == need) {
     picked = band;  // every band expert is in
   } else {
-    long long kd[MAXJ];
+    DD kd[MAXJ];
 #pragma unroll 1
     for (int j = 0; j < MAXJ; ++j) {
-      kd[j] = ORD_NONE;
+      kd[j] = DD{0.0, 0.0};
       const bool mine = (band >> j) & 1u;
-      if (__any_sync(FULL_MASK, mine) && mine) kd[j] = ord64(exact_sigmoid_key(u[j], b[j]));
+      if (__any_sync(FULL_MASK, mine) && mine) kd[j] = dd_sigmoid_key(u[j], b[j]);
     }
     for (int r = 0; r < need; ++r) {
-      long long v = ORD_NONE;
-      int i = NONE;
+      // this lane's best remaining band expert (lowest index among real ties), then the warp's
+      DD v = {0.0, 0.0};
+      int i = -1;
 #pragma unroll 1
       for (int j = 0; j < MAXJ; ++j)
         if (((band & ~picked) >> j) & 1u)
-          if (kd[j] > v || i == NONE) { v = kd[j]; i = j * 32 + lane; }
-      warp_argmax_ord(v, i);
-      if (i == NONE) return false;
+          if (i < 0 || dd_cmp(kd[j], v) < 0) { v = kd[j]; i = j * 32 + lane; }
+      warp_argmax_dd(v, i, i >= 0);
+      if (i < 0) return false;
 #pragma unroll 1
       for (int j = 0; j < MAXJ; ++j)
         if (i == j * 32 + lane) picked |= 1u << j;
@@ -385,31 +541,67 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
   return true;
 }
 
+// fp64 redo of one token (cold): scores and keys in fp64 from the logits ut and the bias, the
+// choice by select_experts<double>. Lane r < K gets the r-th chosen expert in sel_e; false on an
+// internal inconsistency. Reloads its inputs, so the caller's registers stay out of memory.
+__device__ __noinline__ bool redo_fp64(const float* ut, const float* bias, bool sigmoid, int lane,
+                                       int N, int K, int G, int Gk, int topn, int& sel_e) {
+  const int J = (N + 31) >> 5;
+  double u[MAXJ], kd[MAXJ];
+  double umax = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < MAXJ; ++j) {
+    const int e = j * 32 + lane;
+    u[j] = (j < J && e < N) ? (double)ut[e] : -INFINITY;
+    umax = fmax(umax, u[j]);
+  }
+  umax = warp_max(umax);
+  double z = 0.0;
+  if (!sigmoid) {
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) z += (j < J && j * 32 + lane < N) ? exp(u[j] - umax) : 0.0;
+    z = warp_sum(z);
+  }
+#pragma unroll
+  for (int j = 0; j < MAXJ; ++j) {
+    const int e = j * 32 + lane;
+    const bool v = j < J && e < N;
+    const double s = sigmoid ? 1.0 / (1.0 + exp(-u[j])) : exp(u[j] - umax) / z;
+    kd[j] = v ? s + (bias != nullptr ? (double)bias[e] : 0.0) : neg_inf<double>();
+  }
+  const Selection sel = select_experts<double>(kd, lane, N, K, G, Gk, topn, J);
+  sel_e = sel.e;
+  return sel.ok;
+}
+
 __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int J = (a.N + 31) >> 5;
+  const int gsz = a.N / a.G;
   const bool sigmoid = a.score_fn == 1;
-  // Softmax with no selection bias and max-based (or no) group limit: order by the logits.
-  const bool exact_logit_keys = !sigmoid && a.bias == nullptr && (a.G == 1 || a.topn == 1);
+  // Softmax with no selection bias and max-based (or no) group limit: the logits give the order.
+  const bool logit_keys = !sigmoid && a.bias == nullptr && (a.G == 1 || a.topn == 1);
 
+  pdl_wait();
+  pdl_trigger();
   float b[MAXJ];
+  int gj[MAXJ];
 #pragma unroll
   for (int j = 0; j < MAXJ; ++j) {
     const int e = j * 32 + lane;
-    b[j] = (a.bias != nullptr && j < J && e < a.N) ? a.bias[e] : 0.0f;
+    const bool v = j < J && e < a.N;
+    b[j] = (a.bias != nullptr && v) ? a.bias[e] : 0.0f;
+    gj[j] = v ? e / gsz : -1;
   }
 
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < a.T; t += warps) {
     const float* ut = a.u + (size_t)t * a.N;
     float u[MAXJ];
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) {
-      const int e = j * 32 + lane;
-      u[j] = (j < J && e < a.N) ? ut[e] : -INFINITY;
-    }
+    for (int j = 0; j < MAXJ; ++j) u[j] = gj[j] >= 0 ? ut[j * 32 + lane] : -INFINITY;
     // ---- fp32 scores and keys
-    float s[MAXJ], key[MAXJ];
+    float s[MAXJ];
     float umax = u[0];
 #pragma unroll
     for (int j = 1; j < MAXJ; ++j) umax = fmaxf(umax, u[j]);
@@ -425,101 +617,82 @@ __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
 #pragma unroll
       for (int j = 0; j < MAXJ; ++j) s[j] = s[j] / z;
     }
+    uint32_t ok[MAXJ];
+    float kmax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) key[j] = exact_logit_keys ? u[j] : s[j] + b[j];
+    for (int j = 0; j < MAXJ; ++j) {
+      const float key = logit_keys ? u[j] : s[j] + b[j];
+      ok[j] = gj[j] >= 0 ? ord32(key) : 0u;
+      if (gj[j] >= 0) kmax = fmaxf(kmax, fabsf(key));
+    }
 
-    Selection sel = select_experts<float>(key, lane, a.N, a.K, a.G, a.Gk, a.topn, J);
-    bool redo;
-    if (exact_logit_keys) {
-      // Logit order equals exact-probability order except where exp underflows in fp64 or two
-      // distinct logits are so close that their fp64 probabilities may coincide.
-      const double tiny = 1e-9 * fmax(1.0, fabs(sel.kth));
-      redo = !sel.ok || (sel.kth - umax < -600.0) || (a.G > a.Gk && sel.gkth - umax < -600.0) ||
-             (sel.emargin > 0.0 && sel.emargin < tiny) ||
-             (a.G > a.Gk && sel.gmargin > 0.0 && sel.gmargin < 1e-9 * fmax(1.0, fabs(sel.gkth)));
-    } else {
+    const FastSel sel = fast_select(ok, s, gj, lane, a.K, a.G, a.Gk, a.topn);
+    bool redo = !sel.ok;
+    if (!logit_keys && !redo) {
       // A group score is the fp32 sum of its top-n keys: it is off by at most n key errors
       // (the n-th largest of perturbed values moves by at most the largest perturbation) plus
       // the rounding of the sum.
-      float kmax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < MAXJ; ++j)
-        if (j < J && j * 32 + lane < a.N) kmax = fmaxf(kmax, fabsf(key[j]));
       kmax = warp_max(kmax);
-      const double gtol = a.topn * (double)key_tol(kmax) + 6e-8 * fabs(sel.gkth);
-      redo = !sel.ok || sel.emargin <= 2.0 * key_tol(sel.kth) ||
-             (a.G > a.Gk && sel.gmargin <= 2.0 * gtol);
+      const float gtol = a.topn * key_tol(kmax) + 6e-8f * fabsf(sel.gkth);
+      redo = (double)sel.kth - (double)sel.next <= 2.0 * key_tol(sel.kth) ||
+             (a.G > a.Gk && (double)sel.gkth - (double)sel.gnext <= 2.0 * gtol);
     }
-    redo = __any_sync(FULL_MASK, redo);
     int sel_e = sel.e;
-    if (redo && sigmoid && sel.ok && !a.precise_w) {
-      // rescore only the groups and experts within the error bound of a decision
-      int e_ref = -1;
-      if (refine_sigmoid(ut, a.bias, lane, a.N, a.K, a.G, a.Gk, a.topn, sel.gmask, (float)sel.kth,
-                         e_ref)) {
-        sel_e = e_ref;
-        redo = false;
+    float sel_s = sel.se, ssum = sel.ssum;
+    if (redo) {
+      bool settled = false;
+      if (sigmoid && sel.ok)  // rescore only the groups and experts within the error bound
+        settled = refine_sigmoid(ut, a.bias, lane, a.N, a.K, a.G, a.Gk, a.topn, sel.gmask,
+                                 sel.kth, sel_e);
+      if (!settled && !redo_fp64(ut, a.bias, sigmoid, lane, a.N, a.K, a.G, a.Gk, a.topn, sel_e))
+        set_error(a.err, ERR_DEVICE_CHECK);
+      // scores of the chosen experts, from their owner lanes
+      ssum = 0.0f;
+      for (int r = 0; r < a.K; ++r) {
+        const int e = __shfl_sync(FULL_MASK, sel_e, r);
+        float mine = 0.0f;
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j)
+          if (e == j * 32 + lane) mine = s[j];
+        const float v = __shfl_sync(FULL_MASK, mine, e & 31);
+        if (lane == r) sel_s = v;
+        ssum += v;
       }
     }
 
-    // ---- weights: scores of the chosen experts (fp32 unless an fp64 pass is needed)
-    double sd_z = 0.0;  // fp64 softmax normaliser (fp64 passes only)
-    double sel_s = 0.0;
-    const bool need_f64 = redo || a.precise_w;
-    if (need_f64) {
-      double sd[MAXJ];
-      if (sigmoid) {
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j) sd[j] = 1.0 / (1.0 + exp(-(double)u[j]));
-      } else {
-        double z = 0.0;
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j) { sd[j] = exp((double)u[j] - (double)umax); z += sd[j]; }
-        sd_z = warp_sum(z);
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j) sd[j] = sd[j] / sd_z;
-      }
-      if (redo) {
-        double kd[MAXJ];
+    // ---- weights
+    float wv;
+    if (a.precise_w) {
+      // fp64 scores of the chosen experts, rounded once (the v2 drop ranks these values)
+      double z = 0.0;
+      if (!sigmoid) {
 #pragma unroll
         for (int j = 0; j < MAXJ; ++j)
-          kd[j] = (j < J && j * 32 + lane < a.N) ? sd[j] + (double)b[j] : neg_inf<double>();
-        Selection sd_sel = select_experts<double>(kd, lane, a.N, a.K, a.G, a.Gk, a.topn, J);
-        if (!sd_sel.ok) set_error(a.err, ERR_DEVICE_CHECK);
-        sel_e = sd_sel.e;
+          z += gj[j] >= 0 ? exp((double)u[j] - (double)umax) : 0.0;
+        z = warp_sum(z);
       }
-      // fetch s of each chosen expert from its owner lane
+      // the logit of each chosen expert, from its owner lane
+      float ul = 0.0f;
       for (int r = 0; r < a.K; ++r) {
-        const int e = __shfl_sync(FULL_MASK, sel_e, r);
-        double mine = 0.0;
+        const int er = __shfl_sync(FULL_MASK, sel_e, r);
+        float mine = 0.0f;
 #pragma unroll
         for (int j = 0; j < MAXJ; ++j)
-          if (e == j * 32 + lane) mine = sd[j];
-        const double v = __shfl_sync(FULL_MASK, mine, e & 31);
-        if (lane == r) sel_s = v;
+          if (er == j * 32 + lane) mine = u[j];
+        const float v = __shfl_sync(FULL_MASK, mine, er & 31);
+        if (lane == r) ul = v;
       }
-      double denom = warp_sum(lane < a.K ? sel_s : 0.0);
-      double wv = sel_s;
-      if (a.norm_topk) wv = wv / denom;
-      wv = wv * (double)a.scale;
-      sel_s = wv;
+      const double sd = lane < a.K ? (sigmoid ? 1.0 / (1.0 + exp(-(double)ul))
+                                              : exp((double)ul - (double)umax) / z)
+                                   : 0.0;
+      double wd = sd;
+      if (a.norm_topk) wd = wd / warp_sum(sd);
+      wv = (float)(wd * (double)a.scale);
     } else {
-      float mine_s = 0.0f, ss = 0.0f;
-      for (int r = 0; r < a.K; ++r) {
-        const int e = __shfl_sync(FULL_MASK, sel_e, r);
-        mine_s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j)
-          if (e == j * 32 + lane) mine_s = s[j];
-        const float v = __shfl_sync(FULL_MASK, mine_s, e & 31);
-        if (lane == r) ss = v;
-      }
-      float denom = warp_sum(lane < a.K ? ss : 0.0f);
-      float wv = ss;
-      if (a.norm_topk) wv = wv / denom;
-      sel_s = (double)(wv * a.scale);
+      float w32 = sel_s;
+      if (a.norm_topk) w32 = w32 / ssum;
+      wv = w32 * a.scale;
     }
-    if (!sel.ok && !redo) set_error(a.err, ERR_DEVICE_CHECK);
 
     // ---- write in ascending expert order
     int rank = 0;
@@ -530,7 +703,7 @@ __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
     if (lane < a.K) {
       const int e = (sel_e >= 0 && sel_e < a.N) ? sel_e : 0;
       a.idx[(size_t)t * a.K + rank] = e;
-      a.w[(size_t)t * a.K + rank] = (float)sel_s;
+      a.w[(size_t)t * a.K + rank] = wv;
     }
   }
 }
@@ -538,6 +711,8 @@ __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
 // ---------------------------------------------------------------- load statistics
 // Per-block partial sums of the scores of every expert and of lse, lse^2 over its tokens.
 __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8][256];
   __shared__ double redl[8][2];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -597,6 +772,8 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
 
 __global__ void stats_count_kernel(const int32_t* idx, long long n, int N, int32_t* counts,
                                    int* err) {
+  pdl_wait();
+  pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const int e = idx[i];
@@ -607,6 +784,8 @@ __global__ void stats_count_kernel(const int32_t* idx, long long n, int N, int32
 
 // Fixed-order fp64 reduction of the partials: f, P, L_B, L_Z, mean lse.
 __global__ void __launch_bounds__(256) stats_final_kernel(StatsArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ double colsum[256];
   __shared__ double term[256];
   const int e = threadIdx.x;
@@ -645,6 +824,8 @@ __global__ void __launch_bounds__(256) stats_final_kernel(StatsArgs a) {
 
 // Per token: expert counts, and one received token for each distinct device it uses.
 __global__ void group_count_kernel(GroupLossArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int per = a.st.N / a.G;
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < a.st.T; t += gridDim.x * blockDim.x) {
     uint32_t devs = 0;
@@ -664,6 +845,8 @@ __global__ void group_count_kernel(GroupLossArgs a) {
 
 // Fixed-order fp64 reduction: per-expert score sums and counts -> per-device shares -> losses.
 __global__ void __launch_bounds__(256) group_final_kernel(GroupLossArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ double colsum[256];
   __shared__ double tot[1];
   const int e = threadIdx.x, N = a.st.N;
@@ -706,11 +889,10 @@ cudaError_t launch_group_losses(const GroupLossArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   int cb = (a.st.T + 255) / 256;
   if (cb > 1184) cb = 1184;
-  group_count_kernel<<<cb, 256, 0, st>>>(a);
-  stats_partial_kernel<<<a.st.nblk, 256, 0, st>>>(a.st);
-  group_final_kernel<<<1, 256, 0, st>>>(a);
-  note_launches(3);
-  return cudaGetLastError();
+  e = launch_pdl(group_count_kernel, dim3(cb), dim3(256), 0, st, a);
+  if (e == cudaSuccess) e = launch_pdl(stats_partial_kernel, dim3(a.st.nblk), dim3(256), 0, st, a.st);
+  if (e == cudaSuccess) e = launch_pdl(group_final_kernel, dim3(1), dim3(256), 0, st, a);
+  return e;
 }
 
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
@@ -719,9 +901,7 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   int blocks = (warps_needed + 7) / 8;
   const int cap = num_sms * 8;
   if (blocks > cap) blocks = cap;
-  route_kernel<<<blocks, 256, 0, st>>>(a);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(route_kernel, dim3(blocks), dim3(256), 0, st, a);
 }
 
 int stats_blocks(int T) {
@@ -738,11 +918,10 @@ cudaError_t launch_stats(const StatsArgs& a, cudaStream_t st) {
   const long long n = (long long)a.T * a.K;
   int cb = (int)((n + 255) / 256);
   if (cb > 1184) cb = 1184;
-  stats_count_kernel<<<cb, 256, 0, st>>>(a.idx, n, a.N, a.counts, a.err);
-  stats_partial_kernel<<<a.nblk, 256, 0, st>>>(a);
-  stats_final_kernel<<<1, 256, 0, st>>>(a);
-  note_launches(3);
-  return cudaGetLastError();
+  e = launch_pdl(stats_count_kernel, dim3(cb), dim3(256), 0, st, a.idx, n, a.N, a.counts, a.err);
+  if (e == cudaSuccess) e = launch_pdl(stats_partial_kernel, dim3(a.nblk), dim3(256), 0, st, a);
+  if (e == cudaSuccess) e = launch_pdl(stats_final_kernel, dim3(1), dim3(256), 0, st, a);
+  return e;
 }
 
 }  // namespace moe

@@ -31,7 +31,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-fPIC", "-shared", "-ffp-contract=off",
-               _SRC, "-o", tmp]
+               _SRC, "-o", tmp, "-lquadmath"]
         subprocess.check_call(cmd)
         os.replace(tmp, _LIB)
     return _LIB
@@ -49,7 +49,7 @@ def lib():
     global _lib
     if _lib is None:
         _lib = ctypes.CDLL(build())
-        assert _lib.oracle_abi_version() == 1
+        assert _lib.oracle_abi_version() == 2
     return _lib
 
 
@@ -91,16 +91,25 @@ def scores(u, score_fn: str) -> np.ndarray:
     return s
 
 
-def route(cfg, s, select_bias=None):
-    """-> (idx [T,K] int32 ascending expert id, w [T,K] f64, margin [T] f64)."""
+def route(cfg, s, select_bias=None, u=None):
+    """-> (idx [T,K] int32 ascending expert id, w [T,K] f64, margin [T] f64).
+
+    s: the fp64 scores. u (optional): the logits they came from. With u, two keys (or group
+    scores) whose fp64 values lie within 1e-14 * max(1, |a|, |b|) of each other are ordered by
+    their real values, evaluated in quad precision from u (values within 2^-80 * max(|a|, |b|)
+    count as equal: lower index first); without u the fp64 values decide alone."""
     s = _f64(s)
     T = s.shape[0]
     c = _cfg(cfg, T)
     b = None if select_bias is None else _f64(select_bias)
+    uu = None if u is None else _f64(u)
+    if uu is not None:
+        assert uu.shape == s.shape
     idx = np.empty((T, cfg.top_k), np.int32)
     w = np.empty((T, cfg.top_k), np.float64)
     margin = np.empty((T,), np.float64)
-    lib().oracle_route(ctypes.byref(c), _p(s), _p(b), _p(idx, ctypes.c_int32), _p(w), _p(margin))
+    lib().oracle_route(ctypes.byref(c), _p(s), _p(uu), _p(b), _p(idx, ctypes.c_int32), _p(w),
+                       _p(margin))
     return idx, w, margin
 
 
@@ -283,7 +292,7 @@ def layer_forward(cfg, x, w_gate, gate_bias, select_bias, expert_weights, shared
     else:
         u_r = _f64(u)[route_tokens]
     s_r = scores(u_r, cfg.score_fn)
-    idx_r, w_r, margin_r = route(cfg, s_r, select_bias)
+    idx_r, w_r, margin_r = route(cfg, s_r, select_bias, u=u_r)
     kept_r = capacity_drop(cfg.replace(T=len(route_tokens)), idx_r, w_r) if cfg.capacity_drop \
         else np.ones(idx_r.shape, np.uint8)
     res = dict(route_tokens=route_tokens, u=u_r, s=s_r, idx=idx_r, w=w_r, margin=margin_r,

@@ -24,6 +24,8 @@
 #include <cstring>
 #include <vector>
 
+#include <quadmath.h>
+
 extern "C" {
 
 // Layer shape and routing rule. (Own definition: the oracle includes no library header.)
@@ -39,7 +41,7 @@ typedef struct {
   int capacity_drop;    // 1 = v2 device-level token drop
 } oracle_cfg;
 
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }
 
 // Router linear: u[t,e] = sum_h x[t,h] * Wg[e,h] + gb[e]   ([P2] section 5.2 router = nn.Linear)
 void oracle_gate_logits(int T, int H, int N, const double* x, const double* wg, const double* gb,
@@ -91,26 +93,105 @@ void oracle_scores(int T, int N, int score_fn, const double* u, double* s) {
 //   * the K chosen experts are written in ascending expert index (the set is what is defined).
 // margin_out (nullable) gets min(k-th key - (k+1)-th eligible key, Gk-th group score -
 // (Gk+1)-th group score); +inf where no competitor exists.
-static void route_one(const oracle_cfg* c, const double* st, const double* b, int32_t* idx,
-                      double* w, double* margin_out) {
-  const int N = c->N, G = c->G, Gk = c->Gk, K = c->K, gs = c->N / c->G;
-  std::vector<double> key(N);
-  for (int e = 0; e < N; ++e) key[e] = st[e] + (b ? b[e] : 0.0);
+// Keys of one token: fp64 values, and on demand their values in quad precision (__float128)
+// from the logits, used to decide comparisons that fp64 cannot.
+//
+// What the method defines is the order of the real numbers key_e = s_e + b_e (and of group scores,
+// sums of real keys). fp64 evaluation carries a few units in the last place of error (exp, the
+// divisions and sums), so two keys closer than that may compare either way in fp64 depending on
+// the exp implementation. Here two values are compared in fp64 when their fp64 values differ by
+// more than kNear * max(1, |a|, |b|) (far above the fp64 error, so the fp64 order is the real
+// order); otherwise in quad precision (relative error ~1e-33), where values within
+// kTieRel * max(|a|, |b|) of each other count as equal (equal real numbers, e.g.
+// sigmoid(u) + sigmoid(-u) = 1, do not come out exactly equal in any finite precision) and the
+// lower index wins, like exact ties. Without logits the fp64 values decide alone.
+constexpr double kNear = 1e-14;
+constexpr double kTieRel = 0x1p-80;
 
-  // group scores
+struct TokenKeys {
+  const oracle_cfg* c;
+  const double* u;     // logits of the token (nullable)
+  const double* b;     // selection bias (nullable)
+  std::vector<double> key;
+  std::vector<__float128> qkey;
+  std::vector<char> has_q;
+
+  TokenKeys(const oracle_cfg* cfg, const double* st, const double* ut, const double* bias)
+      : c(cfg), u(ut), b(bias), key(cfg->N), qkey(cfg->N), has_q(cfg->N, 0) {
+    for (int e = 0; e < c->N; ++e) key[e] = st[e] + (b ? b[e] : 0.0);
+  }
+  // key_e in quad precision: sigmoid(u) or softmax(u) (max-subtracted), plus the bias
+  __float128 q(int e) {
+    if (!has_q[e]) {
+      __float128 s;
+      if (c->score_fn == 1) {
+        s = 1 / (1 + expq(-(__float128)u[e]));
+      } else {
+        double m = u[0];
+        for (int j = 1; j < c->N; ++j) m = std::max(m, u[j]);
+        __float128 z = 0;
+        for (int j = 0; j < c->N; ++j) z += expq((__float128)u[j] - (__float128)m);
+        s = expq((__float128)u[e] - (__float128)m) / z;
+      }
+      qkey[e] = s + (__float128)(b ? b[e] : 0.0);
+      has_q[e] = 1;
+    }
+    return qkey[e];
+  }
+};
+
+// -1 if a comes first (larger), +1 if b does, 0 if equal (then the caller breaks the tie by
+// index). fa / fb: fp64 values; qa / qb: their quad values, computed only when needed.
+}  // extern "C"
+template <typename QA, typename QB>
+static int compare_values(double fa, double fb, bool refine, QA qa, QB qb) {
+  if (!refine || std::fabs(fa - fb) > kNear * std::max({1.0, std::fabs(fa), std::fabs(fb)}))
+    return fa > fb ? -1 : (fa < fb ? 1 : 0);
+  const __float128 a = qa(), b = qb();
+  const __float128 tie = (__float128)kTieRel * fmaxq(fabsq(a), fabsq(b));
+  if (a - b > tie) return -1;
+  if (b - a > tie) return 1;
+  return 0;
+}
+
+extern "C" {
+static void route_one(const oracle_cfg* c, const double* st, const double* ut, const double* b,
+                      int32_t* idx, double* w, double* margin_out) {
+  const int N = c->N, G = c->G, Gk = c->Gk, K = c->K, gs = c->N / c->G;
+  TokenKeys tk(c, st, ut, b);
+  const std::vector<double>& key = tk.key;
+  const bool refine = ut != nullptr;
+  auto key_before = [&](int a, int bb) {
+    const int r = compare_values(key[a], key[bb], refine, [&] { return tk.q(a); },
+                                 [&] { return tk.q(bb); });
+    return r != 0 ? r < 0 : a < bb;
+  };
+
+  // group scores: the sum of the group's topn largest keys (largest first)
   std::vector<double> gscore(G);
+  std::vector<std::vector<int>> gtop(G);
   for (int g = 0; g < G; ++g) {
-    std::vector<double> v(key.begin() + (size_t)g * gs, key.begin() + (size_t)(g + 1) * gs);
-    std::sort(v.begin(), v.end(), [](double a, double bb) { return a > bb; });
+    std::vector<int> v(gs);
+    for (int j = 0; j < gs; ++j) v[j] = g * gs + j;
+    std::sort(v.begin(), v.end(), key_before);
     double acc = 0.0;
-    for (int j = 0; j < c->topn && j < gs; ++j) acc += v[j];
+    for (int j = 0; j < c->topn && j < gs; ++j) {
+      acc += key[v[j]];
+      gtop[g].push_back(v[j]);
+    }
     gscore[g] = acc;
   }
+  auto gscore_q = [&](int g) {
+    __float128 acc = 0;
+    for (int e : gtop[g]) acc += tk.q(e);
+    return acc;
+  };
   std::vector<int> gorder(G);
   for (int g = 0; g < G; ++g) gorder[g] = g;
   std::sort(gorder.begin(), gorder.end(), [&](int a, int bb) {
-    if (gscore[a] != gscore[bb]) return gscore[a] > gscore[bb];
-    return a < bb;
+    const int r = compare_values(gscore[a], gscore[bb], refine, [&] { return gscore_q(a); },
+                                 [&] { return gscore_q(bb); });
+    return r != 0 ? r < 0 : a < bb;
   });
   std::vector<char> gkeep(G, 0);
   for (int j = 0; j < Gk; ++j) gkeep[gorder[j]] = 1;
@@ -119,10 +200,7 @@ static void route_one(const oracle_cfg* c, const double* st, const double* b, in
   std::vector<int> cand;
   for (int e = 0; e < N; ++e)
     if (gkeep[e / gs]) cand.push_back(e);
-  std::sort(cand.begin(), cand.end(), [&](int a, int bb) {
-    if (key[a] != key[bb]) return key[a] > key[bb];
-    return a < bb;
-  });
+  std::sort(cand.begin(), cand.end(), key_before);
   std::vector<int> chosen(cand.begin(), cand.begin() + K);
   std::sort(chosen.begin(), chosen.end());
 
@@ -142,12 +220,14 @@ static void route_one(const oracle_cfg* c, const double* st, const double* b, in
   }
 }
 
-void oracle_route(const oracle_cfg* c, const double* s, const double* sel_bias, int32_t* idx,
-                  double* w, double* margin) {
+// u (nullable): the logits the scores came from; with them, near ties are decided by the real
+// order of the keys (see TokenKeys), without them by the fp64 scores alone.
+void oracle_route(const oracle_cfg* c, const double* s, const double* u, const double* sel_bias,
+                  int32_t* idx, double* w, double* margin) {
 #pragma omp parallel for schedule(static)
   for (int t = 0; t < c->T; ++t)
-    route_one(c, s + (size_t)t * c->N, sel_bias, idx + (size_t)t * c->K, w + (size_t)t * c->K,
-              margin ? margin + t : nullptr);
+    route_one(c, s + (size_t)t * c->N, u ? u + (size_t)t * c->N : nullptr, sel_bias,
+              idx + (size_t)t * c->K, w + (size_t)t * c->K, margin ? margin + t : nullptr);
 }
 
 // [P3] ST-MoE auxiliary load-balance loss and router Z-loss over a batch of T tokens.

@@ -21,8 +21,9 @@ def _perm_inputs(cfg, seed=3):
     T = cfg.T
     u = make_logits(cfg, seed=seed, T=T)
     sb = make_router(cfg)["select_bias"]
-    s = oracle.scores(u.double().numpy(), cfg.score_fn)
-    idx, w, _ = oracle.route(cfg, s, None if sb is None else sb.double().numpy())
+    u64 = u.double().numpy()
+    s = oracle.scores(u64, cfg.score_fn)
+    idx, w, _ = oracle.route(cfg, s, None if sb is None else sb.double().numpy(), u=u64)
     kept = oracle.capacity_drop(cfg, idx, w) if cfg.capacity_drop else None
     offs, row_token, slot_row = oracle.permute(cfg, idx, kept)
     return idx, w, offs, row_token, slot_row
@@ -148,3 +149,37 @@ def test_tile_schedule_does_not_change_results(name):
     assert moe.moe_get_error() == 0
     assert torch.equal(y_dyn[:R], y_st[:R])
     assert torch.equal(ys_dyn, ys_st)
+
+
+@pytest.mark.parametrize("name", ["mid_a", "mid_odd", "mid_v2", "v3_decode_32", "v3_decode_512",
+                                  "v3_prefill_e32", "v1"])
+def test_row_gather_equals_permuted_copy(name):
+    """The up projection reading its routed rows from x through row_token (tile::gather4 loads,
+    what moe_layer_forward runs) gives bitwise the outputs of the same GEMM on the permuted copy
+    x_perm = x[row_token]: the gather changes where the token rows come from, not the
+    arithmetic. Segments of every length occur (ragged tails, segments shorter than one row
+    group of four, empty experts)."""
+    import mixture_experts_routing_sigmoid_b300 as moe
+    cfg = CFGS[name]
+    T, H, K, I, S = cfg.T, cfg.hidden, cfg.top_k, cfg.inter, cfg.n_shared
+    dev = "cuda"
+    w = make_weights(cfg, device=dev)
+    x = make_x(cfg, device=dev, seed=2)
+    idx, wt, offs, row_token, slot_row = _perm_inputs(cfg)
+    R = int(offs[-1])
+    rt = torch.full((T * K,), -3, dtype=torch.int32, device=dev)  # rows past R: not read
+    rt[:R] = torch.from_numpy(row_token).to(dev)
+    x_perm = torch.zeros((T * K, H), dtype=x.dtype, device=dev)
+    x_perm[:R] = x[rt[:R].long()]
+    offs_d = torch.from_numpy(offs).to(dev)
+    h_ref = torch.zeros((T * K, I), dtype=x.dtype, device=dev)
+    hs_ref = torch.zeros((T, max(S, 1) * I), dtype=x.dtype, device=dev) if S else None
+    moe.moe_expert_up(cfg, T, x_perm, offs_d, x, w, h_ref, hs_ref)
+    h = torch.full_like(h_ref, float("nan"))
+    hs = torch.full_like(hs_ref, float("nan")) if S else None
+    moe.moe_expert_up_gather(cfg, T, x, rt, offs_d, w, h, hs)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error() == 0
+    assert torch.equal(h[:R], h_ref[:R])
+    if S:
+        assert torch.equal(hs, hs_ref)

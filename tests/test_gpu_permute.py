@@ -17,8 +17,9 @@ CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2}
 def _oracle_routing(cfg, T, seed=3):
     u = make_logits(cfg, seed=seed, T=T)
     sb = make_router(cfg)["select_bias"]
-    s = oracle.scores(u.double().numpy(), cfg.score_fn)
-    idx, w, _ = oracle.route(cfg, s, None if sb is None else sb.double().numpy())
+    u64 = u.double().numpy()
+    s = oracle.scores(u64, cfg.score_fn)
+    idx, w, _ = oracle.route(cfg, s, None if sb is None else sb.double().numpy(), u=u64)
     return idx, w
 
 
@@ -92,7 +93,7 @@ def test_permute_end_to_end_from_gpu_route():
     idx_g, w_g, _ = gpu_route(cfg, T, logits=u.cuda(), weights={})
     offs, rt, sr, _ = gpu_permute(cfg, T, idx_g, w_g)
     s = oracle.scores(u.double().numpy(), "softmax")
-    idx_o, w_o, _ = oracle.route(cfg, s)
+    idx_o, w_o, _ = oracle.route(cfg, s, u=u.double().numpy())
     kept = oracle.capacity_drop(cfg, idx_o, w_o)
     offs_o, rt_o, sr_o = oracle.permute(cfg, idx_o, kept)
     np.testing.assert_array_equal(offs.cpu().numpy(), offs_o)

@@ -24,8 +24,9 @@ ROUTE_CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_
 
 
 def _oracle_route(cfg, u, sb):
-    s = oracle.scores(u.double().numpy(), cfg.score_fn)
-    return oracle.route(cfg, s, None if sb is None else sb.double().numpy())
+    u64 = u.double().numpy()
+    s = oracle.scores(u64, cfg.score_fn)
+    return oracle.route(cfg, s, None if sb is None else sb.double().numpy(), u=u64)
 
 
 def _check_route(cfg, u, sb, what=""):
@@ -90,7 +91,7 @@ def test_load_stats(name):
     sb = make_router(cfg)["select_bias"]
     u64 = u.double().numpy()
     s = oracle.scores(u64, cfg.score_fn)
-    idx_o, _, _ = oracle.route(cfg, s, None if sb is None else sb.double().numpy())
+    idx_o, _, _ = oracle.route(cfg, s, None if sb is None else sb.double().numpy(), u=u64)
     st = oracle.load_stats(cfg, u64, s, idx_o)
     counts = torch.empty(N, dtype=torch.int32, device="cuda")
     f = torch.empty(N, dtype=torch.float32, device="cuda")
@@ -129,7 +130,8 @@ def test_route_end_to_end_from_x(name):
         return  # weights / drop are checked with identical logits above
     sb = r["select_bias"]
     s = oracle.scores(u_o, cfg.score_fn)
-    idx_o, w_o, margin = oracle.route(cfg, s, None if sb is None else sb.cpu().double().numpy())
+    idx_o, w_o, margin = oracle.route(cfg, s, None if sb is None else sb.cpu().double().numpy(),
+                                      u=u_o)
     keep = margin >= 1e-4
     n_ex = int((~keep).sum())
     print(f"{name}: {n_ex} of {len(tok)} sampled tokens excluded (margin < 1e-4)")

@@ -5,6 +5,7 @@ a closed form, an invariant stated on the pages, brute-force enumeration on tiny
 or a special case that reduces to a library routine (numpy / scipy / torch on CPU).
 """
 import itertools
+import os
 import math
 
 import numpy as np
@@ -143,6 +144,56 @@ def test_route_invariants(name):
     assert np.all(margin >= 0)
     st = oracle.load_stats(cfg, u, s, idx)
     assert st.counts.sum() == 257 * cfg.top_k
+
+
+def _near_tie_pairs():
+    out = []
+    for line in open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                                  "sigmoid_near_ties.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        ua, ub, D, d = line.split()
+        out.append((float.fromhex(ua), float.fromhex(ub), float.fromhex(D), int(d)))
+    return out
+
+
+def test_route_near_ties_follow_the_real_order():
+    """Keys a few fp64 units apart ("DeepSeek MoE：从v1到v3的演进", DeepSeek-v3: rank by
+    sigmoid(u) + b): given the logits, the oracle orders them as the real numbers are ordered,
+    checked against mpmath at 60 significant digits (independent of the oracle and of any
+    libm exp). Real ties (differences below 2^-80 relative) go to the lower expert."""
+    import mpmath
+    mpmath.mp.dps = 60
+    cfg = CONFIGS["v3_prefill"].replace(n_groups=1, topk_groups=1, top_k=1, n_routed=4)
+    sig = lambda v: 1 / (1 + mpmath.exp(-mpmath.mpf(v)))
+    n_flip = 0
+    for ua, ub, D, _ in _near_tie_pairs():
+        ka, kb = sig(ua), sig(ub) + mpmath.mpf(D)
+        want_a = ka > kb or (abs(ka - kb) <= mpmath.mpf(2) ** -80 * max(ka, kb))  # A: lower index
+        u = np.array([[ua, ub, -8.0, -8.0]])
+        b = np.array([0.0, D, 0.0, 0.0])
+        s = oracle.scores(u, "sigmoid")
+        idx, _, _ = oracle.route(cfg, s, b, u=u)
+        assert idx[0, 0] == (0 if want_a else 1), (ua, ub, D)
+        idx64, _, _ = oracle.route(cfg, s, b)
+        n_flip += int(idx64[0, 0] != idx[0, 0])
+    # fp64 alone is not enough to order these keys: it gets some of them wrong
+    assert n_flip > 0
+
+
+def test_route_real_ties_of_group_scores_go_to_the_lower_group():
+    """sigmoid(u) + sigmoid(-u) = 1 exactly: two groups whose top-2 keys are such pairs tie in
+    the reals (their fp64 sums may differ by a unit), and the lower group wins as for any tie."""
+    cfg = CONFIGS["v3_prefill"].replace(n_routed=8, n_groups=4, topk_groups=1, top_k=2,
+                                        group_score_topn=2)
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        a, c = rng.uniform(0.1, 3.0, size=2).astype(np.float32)
+        u = np.array([[-8, -8, a, -a, c, -c, -8, -8]], np.float64)
+        b = np.zeros(8)
+        s = oracle.scores(u, "sigmoid")
+        idx, _, _ = oracle.route(cfg, s, b, u=u)
+        assert list(idx[0]) == [2, 3]
 
 
 def test_scores_match_scipy():

@@ -23,8 +23,10 @@ from tests.helpers import MID_A, MID_V2
 def _routing(cfg, T, seed):
     u = make_logits(cfg, seed=seed, T=T)
     sb = make_router(cfg)["select_bias"]
-    s = oracle.scores(u.double().numpy(), cfg.score_fn)
-    idx, w, _ = oracle.route(cfg.replace(T=T), s, None if sb is None else sb.double().numpy())
+    u64 = u.double().numpy()
+    s = oracle.scores(u64, cfg.score_fn)
+    idx, w, _ = oracle.route(cfg.replace(T=T), s, None if sb is None else sb.double().numpy(),
+                             u=u64)
     return torch.from_numpy(idx).cuda(), torch.from_numpy(w.astype(np.float32)).cuda()
 
 
