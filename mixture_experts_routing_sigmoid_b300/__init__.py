@@ -21,7 +21,11 @@ __all__ = ["MoeError", "MoeConfig", "MoeWeights", "lib", "make_config", "make_we
            "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT",
            "MOE_ERR_DEVICE_CHECK"]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
+# MOE_B300_CHECKED=1 in the environment loads the bounds-checked build (same entry points; the
+# kernels check segment offsets, rows and slots and report MOE_ERR_DEVICE_CHECK).
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libmoe_b300_checked.so" if os.environ.get("MOE_B300_CHECKED") == "1"
+                        else "libmoe_b300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, -1, -2, -3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK = -4, -5, -6

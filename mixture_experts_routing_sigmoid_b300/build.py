@@ -9,6 +9,9 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe_b300.so")
+# The same library with the kernels' device-side index checks compiled in (-DMOE_CHECKS): an
+# offset, row or slot index outside its range is reported as MOE_ERR_DEVICE_CHECK and skipped.
+LIB_CHECKED = os.path.join(HERE, "libmoe_b300_checked.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
@@ -19,22 +22,29 @@ def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(
         os.path.join(CSRC, "*.h")) + [os.path.join(HERE, "..", "include", "moe.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not (force or _stale()):
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [NVCC, *ARCH, *FLAGS, *(["-Xptxas", "-v"] if verbose else []), *sources(), "-o", tmp]
+def _compile(lib: str, extra: list[str], verbose: bool):
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = [NVCC, *ARCH, *FLAGS, *extra, *(["-Xptxas", "-v"] if verbose else []), *sources(),
+           "-o", tmp]
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Builds libmoe_b300.so and its bounds-checked twin; returns the default library's path."""
+    if force or _stale(LIB):
+        _compile(LIB, [], verbose)
+    if force or _stale(LIB_CHECKED):
+        _compile(LIB_CHECKED, ["-DMOE_CHECKS"], verbose)
     return LIB
 
 

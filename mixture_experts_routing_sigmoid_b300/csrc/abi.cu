@@ -326,6 +326,8 @@ moe_status do_combine(const moe_config* c, int32_t T, const void* y, const int32
   CombineArgs a;
   a.T = T; a.H = c->hidden; a.K = c->top_k; a.dtype = c->dtype;
   a.y = y; a.slot_row = slot_row; a.w = wt; a.ys = y_sh; a.out = out;
+  a.rows = T * c->top_k;
+  a.err = error_word();
   return cuda_status(launch_combine(a, num_sms(), st), "combine");
 }
 

@@ -35,6 +35,10 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
       r[k] = k < K ? __ldg(a.slot_row + (size_t)t * K + k) : -1;
+      if (kChecks && (r[k] < -1 || r[k] >= a.rows)) {
+        set_error(a.err, ERR_DEVICE_CHECK);  // not a row of y: skip it
+        r[k] = -1;
+      }
       wk[k] = k < K ? __ldg(a.w + (size_t)t * K + k) : 0.0f;
     }
     uint4 v[KM];

@@ -18,6 +18,15 @@ __device__ __forceinline__ void set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Index checks of the bounds-checked build (compiled with -DMOE_CHECKS): a kernel that meets a
+// segment offset, row or slot index outside its logical range records ERR_DEVICE_CHECK and skips
+// that access. The default build compiles the checks out.
+#ifdef MOE_CHECKS
+constexpr bool kChecks = true;
+#else
+constexpr bool kChecks = false;
+#endif
+
 // ------------------------------------------------------------------ element types
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }

@@ -56,7 +56,12 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(GemmArgs a) {
   pdl_wait();
   pdl_trigger();
   const int p = blockIdx.z;
-  const Prob q = get_prob(a, p);
+  Prob q = get_prob(a, p);
+  if (kChecks && a.mode != MODE_GATE && p < a.n_routed &&
+      (q.row0 < 0 || q.rows < 0 || q.row0 + q.rows > a.rows_cap)) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) set_error(a.err, ERR_DEVICE_CHECK);
+    return;  // a segment outside the rows: skip the problem
+  }
   const int m0 = blockIdx.y * TM;
   if (m0 >= q.rows) return;
   const bool up = a.mode == MODE_UP;

@@ -73,14 +73,26 @@ constexpr int XBOX_S = 32, XBOX_L = 64;  // token rows per TMA box (small / larg
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;    // 2 s per wait
 constexpr unsigned long long GRACE_NS = 100000000ull;       // drain after an abort
 
-constexpr int TOK = 256;                 // tokens per tile at most (MMA N)
-constexpr int STAGES = 3;
 constexpr int SQ = 4;                    // tile schedule ring slots
 constexpr int A_UNIT = BM * KU * 2;      // this CTA's weight rows, one unit
-constexpr int B_UNIT = TOK / 2 * KU * 2;  // this CTA's token rows (at most), one unit
 constexpr int A_BYTES = UNITS * A_UNIT;
-constexpr int B_BYTES = UNITS * B_UNIT;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+
+// Ring geometry: tokens per tile at most (MMA N) and ring stages. A stage holds a k block of
+// the CTA's weight rows (32 KB) and of its half of the tile's tokens (TOK/2 rows). Fewer tokens
+// per tile leave room for more stages, i.e. more weight bytes in flight per CTA, which is what a
+// tile with few tokens (a weight stream) needs; a tile with many tokens needs the wide MMA.
+//   GEO 0: 256 tokens, 3 stages of 64 KB (any batch; the only one the router GEMM uses)
+//   GEO 1: 128 tokens, 4 stages of 48 KB (batches of at most 128 tokens: one tile per expert)
+//   GEO 2:  64 tokens, 5 stages of 40 KB (batches of at most 64 tokens)
+template <int GEO> struct Geom;
+template <> struct Geom<0> { static constexpr int TOK = 256, STAGES = 3; };
+template <> struct Geom<1> { static constexpr int TOK = 128, STAGES = 4; };
+template <> struct Geom<2> { static constexpr int TOK = 64, STAGES = 5; };
+constexpr int MAX_STAGES = 5, MAX_TOK = 256;
+template <int GEO>  // this CTA's token rows (at most), one unit
+__host__ __device__ constexpr int b_unit() { return Geom<GEO>::TOK / 2 * KU * 2; }
+template <int GEO>
+__host__ __device__ constexpr int stage_bytes() { return A_BYTES + UNITS * b_unit<GEO>(); }
 
 struct TcParams {
   CUtensorMap tmW0, tmW1;    // weights: routed, shared (box 128 rows; UP: interleaved 5-D box)
@@ -89,6 +101,7 @@ struct TcParams {
   CUtensorMap tmXg;          // UP with row gather: x [T, H], box one row high (tile::gather4)
   const int32_t* row_token;  // UP with row gather: token of each routed row, else nullptr
   const int32_t* offsets;
+  int rows_cap;              // rows of the routed activation and output tensors
   int n_routed, has_shared, T, H, I, S, N;
   void* out0;
   void* out1;
@@ -119,8 +132,8 @@ constexpr int TILE_WORDS = sizeof(Tile) / 4;
 static_assert(TILE_WORDS == 12, "a tile travels as three 16-byte vectors");
 
 struct SmemCtl {
-  uint64_t full[STAGES];       // first CTA's copy counts both CTAs' loads
-  uint64_t empty[STAGES];      // per CTA, arrived on by the MMA commit
+  uint64_t full[MAX_STAGES];   // first CTA's copy counts both CTAs' loads
+  uint64_t empty[MAX_STAGES];  // per CTA, arrived on by the MMA commit
   uint64_t tfull[2];           // per CTA, arrived on by the MMA commit
   uint64_t tempty[2];          // first CTA's copy: 4 epilogue warps x 2 CTAs
   uint64_t drain;
@@ -133,7 +146,7 @@ struct SmemCtl {
   uint64_t took;               // first CTA: its producer has started the last published tile
   Tile lsq[SQ];
   Tile xq[SQ];
-  int grow[SQ][TOK / 2];      // row gather: x row of each of this CTA's token rows of lsq[slot]
+  int grow[SQ][MAX_TOK / 2];  // row gather: x row of each of this CTA's token rows of lsq[slot]
   uint32_t tmem_base;
   int abort_flag;
   int nprob;
@@ -144,8 +157,10 @@ struct SmemCtl {
   int row0[MAXP];
 };
 
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
-static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
+template <int GEO>
+constexpr size_t smem_bytes() { return (size_t)Geom<GEO>::STAGES * stage_bytes<GEO>() + sizeof(SmemCtl); }
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448,
+              "shared memory budget of one CTA");
 
 template <int MODE>
 __device__ __forceinline__ int feat_total(const TcParams& p, bool shared) {
@@ -167,8 +182,9 @@ __device__ __forceinline__ int k_units_of(const TcParams& p, bool shared) {
   return p.H / KU;
 }
 
-template <int MODE>
+template <int MODE, int GEO>
 __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c, int tile) {
+  constexpr int TOK = Geom<GEO>::TOK;
   int lo = 0, hi = c.nprob - 1;  // largest q with tile_start[q] <= tile
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -336,6 +352,7 @@ __device__ __forceinline__ void fill_rows(SmemCtl& c, uint32_t qs, const TcParam
   for (int i = threadIdx.x & 31; i < half; i += 32) {
     const int r = base + i;
     const int tok = r < end ? __ldg(p.row_token + r) : pad;
+    if (kChecks && (tok < 0 || tok >= p.T)) set_error(p.err, ERR_DEVICE_CHECK);
     c.grow[qs][i] = min(max(tok, 0), p.T - 1);
   }
   __threadfence_block();
@@ -417,8 +434,10 @@ __device__ __forceinline__ bool ring_take_warp(SmemCtl& c, uint32_t qs, uint32_t
   return true;
 }
 
-template <int MODE>
+template <int MODE, int GEO>
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  constexpr int TOK = Geom<GEO>::TOK, STAGES = Geom<GEO>::STAGES;
+  constexpr int B_UNIT = b_unit<GEO>(), STAGE_BYTES = stage_bytes<GEO>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);  // 128-byte swizzle atoms want 1 KB alignment
   uint8_t* sgen = smem_raw;
@@ -463,7 +482,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     int rows = p.T, row0 = 0;
     if (MODE != MODE_GATE && q < p.n_routed) {
       row0 = p.offsets[q];
-      rows = max(p.offsets[q + 1] - row0, 0);
+      const int end = p.offsets[q + 1];
+      rows = max(end - row0, 0);
+      if (kChecks && (row0 < 0 || end < row0 || end > p.rows_cap)) {
+        set_error(p.err, ERR_DEVICE_CHECK);  // a segment outside the rows: skip the problem
+        row0 = 0;
+        rows = 0;
+      }
     }
     c.rows[q] = rows;
     c.row0[q] = row0;
@@ -679,7 +704,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       Tile t;
       const TcParams* gp = (MODE == MODE_UP && p.row_token != nullptr) ? &p : nullptr;
       if (rank == 0) {
-        t = cur < total ? decode_tile<MODE>(p, c, cur) : end_tile();
+        t = cur < total ? decode_tile<MODE, GEO>(p, c, cur) : end_tile();
         if (!ring_publish(c, qs, qph, t, abort_flag, p.err, gp, rank) ||
             !ring_send(c, qs, qph, t, abort_flag, p.err))
           break;
@@ -855,7 +880,7 @@ bool make_token_maps(CUtensorMap* big, CUtensorMap* small, const void* base, uin
   return make_map(big, base, inner, outer, XBOX_L) && make_map(small, base, inner, outer, XBOX_S);
 }
 
-template <int MODE>
+template <int MODE, int GEO>
 cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
   static int grid_for_device[64] = {0};
   int dev = 0;
@@ -871,19 +896,19 @@ cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_bytes<GEO>();
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   if (grid == 0) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE, GEO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)smem_bytes<GEO>());
     if (e != cudaSuccess) return e;
     // persistent grid: as many CTA pairs as can be resident at once (one CTA per SM)
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<MODE>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<MODE, GEO>, &cfg);
     if (e != cudaSuccess) return e;
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     grid = 2 * (clusters < num_sms / 2 ? clusters : num_sms / 2);
@@ -891,7 +916,15 @@ cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
   }
   cfg.gridDim = dim3(grid, 1, 1);
   note_launches(1);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, prm);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, GEO>, prm);
+}
+
+// Expert GEMMs: the ring geometry follows the batch (a segment never has more rows than T).
+template <int MODE>
+cudaError_t launch_geo(const TcParams& prm, int num_sms, cudaStream_t st) {
+  if (prm.T <= Geom<2>::TOK) return launch_mode<MODE, 2>(prm, num_sms, st);
+  if (prm.T <= Geom<1>::TOK) return launch_mode<MODE, 1>(prm, num_sms, st);
+  return launch_mode<MODE, 0>(prm, num_sms, st);
 }
 
 }  // namespace
@@ -901,6 +934,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.offsets = a.offsets;
+  prm.rows_cap = a.rows_cap;
   prm.n_routed = a.n_routed;
   prm.has_shared = a.has_shared;
   prm.T = a.T; prm.H = a.H; prm.I = a.I; prm.S = a.S; prm.N = a.N;
@@ -916,7 +950,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
     if (!ok) return cudaErrorInvalidValue;
     // Few token tiles (decode): split the K range so that about every CTA pair has a tile;
     // the partial sums go to the caller's scratch and are reduced in a fixed order.
-    const int tiles = (int)((T + TOK - 1) / TOK) * (int)((N + 2 * BM - 1) / (2 * BM));
+    const int tiles = (int)((T + Geom<0>::TOK - 1) / Geom<0>::TOK) * (int)((N + 2 * BM - 1) / (2 * BM));
     const int ku_total = (int)(H / KU);
     const int kb_total = (ku_total + UNITS - 1) / UNITS;
     const int pairs = num_sms / 2;
@@ -932,7 +966,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
         prm.gate_part = a.gate_part;
       }
     }
-    cudaError_t e = launch_mode<MODE_GATE>(prm, num_sms, st);
+    cudaError_t e = launch_mode<MODE_GATE, 0>(prm, num_sms, st);
     if (e != cudaSuccess || prm.splits == 1) return e;
     int blocks = (int)(((size_t)T * N + 255) / 256);
     if (blocks > num_sms * 8) blocks = num_sms * 8;
@@ -953,14 +987,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
     if (a.has_shared) ok = ok && make_up_weight_map(&prm.tmW1, a.b1, H, I, S) &&
                            make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, H, T);
     if (!ok) return cudaErrorInvalidValue;
-    return launch_mode<MODE_UP>(prm, num_sms, st);
+    return launch_geo<MODE_UP>(prm, num_sms, st);
   }
   if (a.n_routed > 0) ok = ok && make_map(&prm.tmW0, a.b0, I, N * H, BM) &&
                            make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, I, R);
   if (a.has_shared) ok = ok && make_map(&prm.tmW1, a.b1, I, S * H, BM) &&
                          make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, S * I, T);
   if (!ok) return cudaErrorInvalidValue;
-  return launch_mode<MODE_DOWN>(prm, num_sms, st);
+  return launch_geo<MODE_DOWN>(prm, num_sms, st);
 }
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long timeout_ns, cudaStream_t st) {

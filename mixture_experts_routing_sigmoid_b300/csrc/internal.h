@@ -120,6 +120,8 @@ cudaError_t launch_dispatch(const PermuteArgs& a, int num_sms, cudaStream_t st);
 // ---------------------------------------------------------------- combine (combine.cu)
 struct CombineArgs {
   int T, H, K, dtype;
+  int rows;             // rows of y (slot_row values are below it)
+  int* err;
   const void* y;        // [rows, H]
   const int32_t* slot_row;
   const float* w;

@@ -28,52 +28,108 @@ __device__ __forceinline__ unsigned long long drop_key(float w, long long a) {
          static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(a));
 }
 
-__global__ void __launch_bounds__(1024) drop_threshold_kernel(PermuteArgs p) {
+// One CTA per device: radix select, 8 bits per pass from the top, of the C-th largest key among
+// the device's assignments. A first pass over all assignments (loads batched so that many are in
+// flight) collects the device's keys into shared memory, up to DROP_SMEM_KEYS of them; each radix
+// pass then histograms the keys that match the bits chosen so far, every warp into a histogram
+// of its own (no contention between warps), and a parallel suffix scan over the 256 bins picks
+// the bin holding the C-th key. A device with more keys than fit streams them from global memory
+// on every pass instead (same arithmetic).
+constexpr int DROP_THREADS = 1024;
+constexpr int DROP_WARPS = DROP_THREADS / 32;
+constexpr int DROP_SMEM_KEYS = 20480;  // 160 KB of 64-bit keys
+constexpr int DROP_BATCH = 8;          // assignments per thread per load batch
+
+__global__ void __launch_bounds__(DROP_THREADS) drop_threshold_kernel(PermuteArgs p) {
   pdl_wait();
   pdl_trigger();
-  __shared__ unsigned int hist[256];
+  extern __shared__ unsigned long long skey[];          // [DROP_SMEM_KEYS]
+  __shared__ unsigned int whist[DROP_WARPS][256];       // per-warp histograms
+  __shared__ unsigned int wsum[8];
   __shared__ unsigned long long s_prefix;
   __shared__ long long s_remaining;
   __shared__ unsigned int s_count;
   const int d = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int per = p.N / p.D;
   const long long A = (long long)p.T * p.K;
   const long long C = (A + p.D - 1) / p.D;
   if (threadIdx.x == 0) s_count = 0;
   __syncthreads();
-  unsigned int mine = 0;
-  for (long long a = threadIdx.x; a < A; a += blockDim.x)
-    if (p.idx[a] / per == d) ++mine;
-  atomicAdd(&s_count, mine);
+  // ---- collect this device's keys (every lane runs the same number of iterations)
+  const long long step = (long long)DROP_THREADS * DROP_BATCH;
+  for (long long a0 = 0; a0 < A; a0 += step) {
+    int e[DROP_BATCH];
+#pragma unroll
+    for (int i = 0; i < DROP_BATCH; ++i) {
+      const long long a = a0 + (long long)i * DROP_THREADS + threadIdx.x;
+      e[i] = a < A ? __ldg(p.idx + a) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < DROP_BATCH; ++i) {
+      const long long a = a0 + (long long)i * DROP_THREADS + threadIdx.x;
+      const bool mine = e[i] >= 0 && e[i] / per == d;
+      const unsigned int bal = __ballot_sync(FULL_MASK, mine);
+      unsigned int base = 0;
+      if (lane == 0 && bal != 0u) base = atomicAdd(&s_count, (unsigned int)__popc(bal));
+      base = __shfl_sync(FULL_MASK, base, 0);
+      if (mine) {
+        const unsigned int pos = base + __popc(bal & ((1u << lane) - 1u));
+        if (pos < (unsigned int)DROP_SMEM_KEYS) skey[pos] = drop_key(__ldg(p.w + a), a);
+      }
+    }
+  }
   __syncthreads();
-  if ((long long)s_count <= C) {
+  const long long n = s_count;
+  if (n <= C) {
     if (threadIdx.x == 0) p.thr[d] = 0ull;  // every key is >= 0: keep all
     return;
   }
+  const bool in_smem = n <= DROP_SMEM_KEYS;
   if (threadIdx.x == 0) { s_prefix = 0ull; s_remaining = C; }
-  __syncthreads();
+  unsigned int* hist = whist[wid];
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
     const unsigned long long hi_mask = (pass == 0) ? 0ull : (~0ull << (shift + 8));
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    for (int i = threadIdx.x; i < DROP_WARPS * 256; i += DROP_THREADS) (&whist[0][0])[i] = 0;
     __syncthreads();
     const unsigned long long prefix = s_prefix;
-    for (long long a = threadIdx.x; a < A; a += blockDim.x) {
-      if (p.idx[a] / per != d) continue;
-      const unsigned long long key = drop_key(p.w[a], a);
-      if ((key & hi_mask) != prefix) continue;
-      atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    const long long rem = s_remaining;
+    if (in_smem) {
+      for (long long i = threadIdx.x; i < n; i += DROP_THREADS) {
+        const unsigned long long key = skey[i];
+        if ((key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+    } else {
+      for (long long a = threadIdx.x; a < A; a += DROP_THREADS) {
+        if (__ldg(p.idx + a) / per != d) continue;
+        const unsigned long long key = drop_key(__ldg(p.w + a), a);
+        if ((key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      long long rem = s_remaining, cum = 0;
-      int bin = 0;
-      for (int b = 255; b >= 0; --b) {
-        if (cum + (long long)hist[b] >= rem) { bin = b; break; }
-        cum += hist[b];
+    // thread t < 256 takes bin 255 - t (summed over the warps' histograms): an inclusive scan
+    // over t gives the keys in bins >= it
+    unsigned int v = 0, incl = 0;
+    if (threadIdx.x < 256) {
+      const int bin = 255 - threadIdx.x;
+      for (int w = 0; w < DROP_WARPS; ++w) v += whist[w][bin];
+      incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int x = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += x;
       }
-      s_prefix = prefix | (static_cast<unsigned long long>(bin) << shift);
-      s_remaining = rem - cum;
+      if (lane == 31) wsum[wid] = incl;
+    }
+    __syncthreads();
+    if (threadIdx.x < 256) {
+      for (int w = 0; w < wid; ++w) incl += wsum[w];
+      const long long above = (long long)(incl - v);  // keys in the bins above this one
+      if (above < rem && (long long)incl >= rem) {     // the C-th key lies in this bin
+        s_prefix = prefix | (static_cast<unsigned long long>(255 - threadIdx.x) << shift);
+        s_remaining = rem - above;
+      }
     }
     __syncthreads();
   }
@@ -253,6 +309,10 @@ __global__ void __launch_bounds__(256) dispatch_rows_kernel(PermuteArgs p) {
     const int32_t* sr = p.slot_row + (size_t)t * p.K;
     for (int k = 0; k < p.K; ++k) {
       const int r = __ldg(sr + k);
+      if (kChecks && (r < -1 || r >= p.T * p.K)) {
+        set_error(p.err, ERR_DEVICE_CHECK);  // not a row of x_perm: skip it
+        continue;
+      }
       if (r >= 0) st_v4(dst + (size_t)r * row_bytes + (size_t)c * 16, v);
     }
   }
@@ -269,7 +329,18 @@ cudaError_t launch_permute(const PermuteArgs& p, int num_sms, cudaStream_t st) {
   }
   const int nb = permute_blocks(p.T);
   if (p.capacity_drop) {
-    const cudaError_t e = launch_pdl(drop_threshold_kernel, dim3(p.D), dim3(1024), 0, st, p);
+    static bool smem_set[64] = {false};  // the attribute is set once per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !smem_set[dev]) {
+      const cudaError_t ea = cudaFuncSetAttribute(
+          drop_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          (int)(DROP_SMEM_KEYS * sizeof(unsigned long long)));
+      if (ea != cudaSuccess) return ea;
+      if (dev >= 0 && dev < 64) smem_set[dev] = true;
+    }
+    const cudaError_t e = launch_pdl(drop_threshold_kernel, dim3(p.D), dim3(DROP_THREADS),
+                                     DROP_SMEM_KEYS * sizeof(unsigned long long), st, p);
     if (e != cudaSuccess) return e;
   }
   if (p.T <= SB_MAX_T) {

@@ -70,11 +70,14 @@ __device__ __forceinline__ float unord32(uint32_t o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
 }
 
-__device__ __forceinline__ float key_tol(float v) {
-  // Bound on |fp32 key - real key|: a sigmoid or softmax score carries a few ulps of error
-  // (expf <= 2 ulp, one IEEE division, one sum), the + bias one rounding; 2e-6 * max(1,|v|)
-  // is several times that bound.
-  return 2e-6f * fmaxf(1.0f, fabsf(v));
+// Bound on |fp32 key - real key| for keys of magnitude at most |v| (or 1).
+//   sigmoid: expf is within 2 ulp (2.4e-7 relative), 1 + e and the IEEE division add 6e-8
+//   each, so s is within 3.6e-7 (absolute, s < 1); + b adds half an ulp of the key: 4.2e-7 in
+//   all for |key| <= 1, bounded here by 5e-7 * max(1, |v|).
+//   softmax: besides the exp, the normaliser is a sum of up to 256 terms (8 per lane, then a
+//   5-level warp tree), within 1e-6 relative; 2e-6 * max(1, |v|) bounds the score's error.
+__device__ __forceinline__ float key_tol(float v, bool sigmoid) {
+  return (sigmoid ? 5e-7f : 2e-6f) * fmaxf(1.0f, fabsf(v));
 }
 
 // ---------------------------------------------------------------- fp32 choice (redux)
@@ -312,10 +315,17 @@ __device__ __noinline__ DD dd_exp(double x) {
   DD r = dd_add(DD{x, 0.0}, dd_neg(dd_mul_d(ln2, k)));
   r.hi *= 0x1p-9;
   r.lo *= 0x1p-9;
+  // 1/n for n = 2..10 as double-double pairs (rounded to nearest, the rest in the low part)
+  const double inv_hi[9] = {0x1p-1, 0x1.5555555555555p-2, 0x1p-2, 0x1.999999999999ap-3,
+                            0x1.5555555555555p-3, 0x1.2492492492492p-3, 0x1p-3,
+                            0x1.c71c71c71c71cp-4, 0x1.999999999999ap-4};
+  const double inv_lo[9] = {0.0, 0x1.5555555555555p-56, 0.0, -0x1.999999999999ap-57,
+                            0x1.5555555555555p-57, 0x1.2492492492492p-57, 0.0,
+                            0x1.c71c71c71c71cp-58, -0x1.999999999999ap-58};
   DD p = r, s = r;
 #pragma unroll 1
   for (int n = 2; n <= 10; ++n) {
-    p = dd_div(dd_mul(p, r), DD{(double)n, 0.0});
+    p = dd_mul(dd_mul(p, r), DD{inv_hi[n - 2], inv_lo[n - 2]});
     s = dd_add(s, p);
   }
 #pragma unroll 1
@@ -358,12 +368,43 @@ __device__ __forceinline__ void warp_argmax_dd(DD& v, int& i, bool valid) {
   }
 }
 
+// fp64 key sigmoid(u) + b: within a few units in the last place of the real key (one out-of-line
+// copy: the recheck runs for a handful of tokens per launch, with its code fetched cold).
+__device__ __noinline__ double sigmoid_key64(float u, float b) {
+  return 1.0 / (1.0 + exp(-(double)u)) + (double)b;
+}
+// fp64 keys (and sums of two) carry a few units in the last place of error, far below this
+// distance; two fp64 values closer than it are ordered in double-double instead.
+__device__ __forceinline__ bool near64(double a, double b) {
+  return fabs(a - b) <= 1e-14 * fmax(1.0, fmax(fabs(a), fabs(b)));
+}
+// Order-preserving map of a (non-NaN) double onto a signed 64-bit integer: comparisons of the
+// fp64 keys run on the integer pipes instead of the (slow) fp64 one.
+__device__ __forceinline__ long long ord64(double d) {
+  const long long i = __double_as_longlong(d);
+  return i >= 0 ? i : i ^ 0x7fffffffffffffffll;
+}
+constexpr long long ORD_NONE = (long long)0x8000000000000000ull;  // below every ord64
+__device__ __forceinline__ double unord64(long long o) {
+  return __longlong_as_double(o >= 0 ? o : o ^ 0x7fffffffffffffffll);
+}
+// Warp-wide argmax on (ordered key desc, index asc); result in every lane.
+__device__ __forceinline__ void warp_argmax_ord(long long& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long ov = __shfl_xor_sync(FULL_MASK, v, o);
+    const int oi = __shfl_xor_sync(FULL_MASK, i, o);
+    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+  }
+}
+
 // Exact selection for a sigmoid gate whose fp32 decision lies within its error bound. Every fp32
 // key is within tol of its real value and every fp32 group score within gtol, so a group whose
 // fp32 score exceeds the Gk-th by more than 2 gtol is among the real best Gk, one below it by more
-// than 2 gtol is not, and only the groups inside that band are rescored in double-double (all
-// their experts) when the band holds more groups than places left; likewise for the experts
-// around the K-th eligible key with 2 tol. The band's members are ranked by their real values
+// than 2 gtol is not, and only the groups inside that band are rescored (all their experts) when
+// the band holds more groups than places left; likewise for the experts around the K-th eligible
+// key with 2 tol. The band is ranked by fp64 keys first; only when the fp64 values on both sides
+// of the cut are within near64() of each other is the band ranked again by double-double values
 // (dd_cmp; ties: lower index). The fp32 keys are recomputed here from the logits exactly as the
 // fp32 pass computes them. Lane r < K receives the r-th chosen expert; false if a rank is missing.
 // fp_gmask and fp_kth are the fp32 pass's chosen groups and K-th key: when the groups stand, its
@@ -397,7 +438,7 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
     }
     const uint32_t at = __ballot_sync(FULL_MASK, lane < G && rnk == Gk - 1);
     const double vg = (double)__shfl_sync(FULL_MASK, gs, __ffs(at) - 1);
-    const double gtol = topn * (double)key_tol((float)kmax) + 6e-8 * fabs(vg);
+    const double gtol = topn * (double)key_tol(kmax, true) + 6e-8 * fabs(vg);
     const bool in = lane < G && (double)gs > vg + 2.0 * gtol;
     const uint32_t cin = __ballot_sync(FULL_MASK, in);
     const uint32_t band = __ballot_sync(FULL_MASK, lane < G && !in && (double)gs >= vg - 2.0 * gtol);
@@ -406,54 +447,90 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
     if (__popc(band) == need) {
       picked = band;  // every band group is in: no exact score needed
     } else {
-      DD gx = {0.0, 0.0};  // lane g: real score of band group g
+      // fp64 scores of the band groups (lane g: group g's, ordered)
+      long long gx = ORD_NONE;
       for (uint32_t m = band; m; m &= m - 1) {
         const int g = __ffs(m) - 1;
-        // the group's top-n real keys: lane-local top-2, then a warp top-2
-        DD a1 = {0.0, 0.0}, a2 = {0.0, 0.0};
-        bool h1 = false, h2 = false;
+        long long a1 = ORD_NONE, a2 = ORD_NONE;
 #pragma unroll 1
         for (int j = 0; j < MAXJ; ++j) {
           const int e = j * 32 + lane;
           const bool mine = j < J && e < N && e / gsz == g;
           if (__any_sync(FULL_MASK, mine) && mine) {
-            const DD k = dd_sigmoid_key(u[j], b[j]);
-            if (!h1 || dd_cmp(k, a1) < 0) { a2 = a1; h2 = h1; a1 = k; h1 = true; }
-            else if (!h2 || dd_cmp(k, a2) < 0) { a2 = k; h2 = true; }
+            const long long o = ord64(sigmoid_key64(u[j], b[j]));
+            if (o > a1) { a2 = a1; a1 = o; } else if (o > a2) { a2 = o; }
           }
         }
-#pragma unroll 1
-        for (int o = 16; o > 0; o >>= 1) {
-          DD b1, b2;
-          b1.hi = __shfl_xor_sync(FULL_MASK, a1.hi, o);
-          b1.lo = __shfl_xor_sync(FULL_MASK, a1.lo, o);
-          b2.hi = __shfl_xor_sync(FULL_MASK, a2.hi, o);
-          b2.lo = __shfl_xor_sync(FULL_MASK, a2.lo, o);
-          const bool g1 = __shfl_xor_sync(FULL_MASK, h1, o);
-          const bool g2 = __shfl_xor_sync(FULL_MASK, h2, o);
-          // merge the two sorted pairs (a1 >= a2, b1 >= b2) into the top two
-          if (g1 && (!h1 || dd_cmp(b1, a1) < 0)) {
-            // b1 is the largest; the second is the larger of a1 and b2
-            const bool second_b2 = g2 && (!h1 || dd_cmp(b2, a1) < 0);
-            a2 = second_b2 ? b2 : a1;
-            h2 = second_b2 ? true : h1;
-            a1 = b1;
-            h1 = true;
-          } else if (g1 && (!h2 || dd_cmp(b1, a2) < 0)) {
-            a2 = b1;
-            h2 = true;
-          }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {  // top-2 of the group, compared as integers
+          const long long b1 = __shfl_xor_sync(FULL_MASK, a1, o);
+          const long long b2 = __shfl_xor_sync(FULL_MASK, a2, o);
+          if (b1 > a1) { a2 = max(a1, b2); a1 = b1; }
+          else { a2 = max(a2, b1); }
         }
-        const DD score = (topn == 1 || !h2) ? a1 : dd_add(a1, a2);
-        if (lane == g) gx = score;
+        if (lane == g) gx = ord64(topn == 1 ? unord64(a1) : unord64(a1) + unord64(a2));
       }
-      for (int r = 0; r < need; ++r) {
+      long long v_cut = ORD_NONE, v_next = ORD_NONE;
+      for (int r = 0; r <= need; ++r) {
         const bool cand = ((band & ~picked) >> lane) & 1u;
-        DD v = gx;
-        int i = lane;
-        warp_argmax_dd(v, i, cand);
-        if (i < 0) return false;
+        long long v = cand ? gx : ORD_NONE;
+        int i = cand ? lane : 0x7fffffff;
+        warp_argmax_ord(v, i);
+        if (r == need) { v_next = v; break; }
+        if (i == 0x7fffffff) return false;
         picked |= 1u << i;
+        v_cut = v;
+      }
+      if (v_next != ORD_NONE && v_cut != ORD_NONE && near64(unord64(v_cut), unord64(v_next))) {
+        // fp64 cannot settle the cut: real scores of the band groups in double-double
+        DD gd = {0.0, 0.0};
+        for (uint32_t m = band; m; m &= m - 1) {
+          const int g = __ffs(m) - 1;
+          DD a1 = {0.0, 0.0}, a2 = {0.0, 0.0};
+          bool h1 = false, h2 = false;
+#pragma unroll 1
+          for (int j = 0; j < MAXJ; ++j) {
+            const int e = j * 32 + lane;
+            const bool mine = j < J && e < N && e / gsz == g;
+            if (__any_sync(FULL_MASK, mine) && mine) {
+              const DD k = dd_sigmoid_key(u[j], b[j]);
+              if (!h1 || dd_cmp(k, a1) < 0) { a2 = a1; h2 = h1; a1 = k; h1 = true; }
+              else if (!h2 || dd_cmp(k, a2) < 0) { a2 = k; h2 = true; }
+            }
+          }
+#pragma unroll 1
+          for (int o = 16; o > 0; o >>= 1) {
+            DD b1, b2;
+            b1.hi = __shfl_xor_sync(FULL_MASK, a1.hi, o);
+            b1.lo = __shfl_xor_sync(FULL_MASK, a1.lo, o);
+            b2.hi = __shfl_xor_sync(FULL_MASK, a2.hi, o);
+            b2.lo = __shfl_xor_sync(FULL_MASK, a2.lo, o);
+            const bool g1 = __shfl_xor_sync(FULL_MASK, h1, o);
+            const bool g2 = __shfl_xor_sync(FULL_MASK, h2, o);
+            // merge the two sorted pairs (a1 >= a2, b1 >= b2) into the top two
+            if (g1 && (!h1 || dd_cmp(b1, a1) < 0)) {
+              const bool second_b2 = g2 && (!h1 || dd_cmp(b2, a1) < 0);
+              a2 = second_b2 ? b2 : a1;
+              h2 = second_b2 ? true : h1;
+              a1 = b1;
+              h1 = true;
+            } else if (g1 && (!h2 || dd_cmp(b1, a2) < 0)) {
+              a2 = b1;
+              h2 = true;
+            }
+          }
+          const DD score = (topn == 1 || !h2) ? a1 : dd_add(a1, a2);
+          if (lane == g) gd = score;
+        }
+        picked = 0;
+        for (int r = 0; r < need; ++r) {
+          const bool cand = ((band & ~picked) >> lane) & 1u;
+          DD v = gd;
+          int i = lane;
+          warp_argmax_dd(v, i, cand);
+          if (i < 0) return false;
+          picked |= 1u << i;
+        }
       }
     }
     gmask = cin | picked;
@@ -481,7 +558,7 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
       if (i == j * 32 + lane) taken |= 1u << j;
     vk = v;
   }
-  const double tol = 2.0 * (double)key_tol(vk);
+  const double tol = 2.0 * (double)key_tol(kmax, true);
   uint32_t cin = 0, band = 0;
 #pragma unroll 1
   for (int j = 0; j < MAXJ; ++j) {
@@ -496,26 +573,53 @@ __device__ __noinline__ bool refine_sigmoid(const float* ut, const float* bias, 
   if (warp_sum(__popc(band)) == need) {
     picked = band;  // every band expert is in
   } else {
-    DD kd[MAXJ];
+    long long kx[MAXJ];
 #pragma unroll 1
     for (int j = 0; j < MAXJ; ++j) {
-      kd[j] = DD{0.0, 0.0};
+      kx[j] = ORD_NONE;
       const bool mine = (band >> j) & 1u;
-      if (__any_sync(FULL_MASK, mine) && mine) kd[j] = dd_sigmoid_key(u[j], b[j]);
+      if (__any_sync(FULL_MASK, mine) && mine) kx[j] = ord64(sigmoid_key64(u[j], b[j]));
     }
-    for (int r = 0; r < need; ++r) {
-      // this lane's best remaining band expert (lowest index among real ties), then the warp's
-      DD v = {0.0, 0.0};
-      int i = -1;
+    long long v_cut = ORD_NONE, v_next = ORD_NONE;
+    for (int r = 0; r <= need; ++r) {
+      long long v = ORD_NONE;
+      int i = 0x7fffffff;
 #pragma unroll 1
       for (int j = 0; j < MAXJ; ++j)
         if (((band & ~picked) >> j) & 1u)
-          if (i < 0 || dd_cmp(kd[j], v) < 0) { v = kd[j]; i = j * 32 + lane; }
-      warp_argmax_dd(v, i, i >= 0);
-      if (i < 0) return false;
+          if (kx[j] > v || i == 0x7fffffff) { v = kx[j]; i = j * 32 + lane; }
+      warp_argmax_ord(v, i);
+      if (r == need) { v_next = v; break; }
+      if (i == 0x7fffffff) return false;
 #pragma unroll 1
       for (int j = 0; j < MAXJ; ++j)
         if (i == j * 32 + lane) picked |= 1u << j;
+      v_cut = v;
+    }
+    if (v_next != ORD_NONE && v_cut != ORD_NONE && near64(unord64(v_cut), unord64(v_next))) {
+      // fp64 cannot settle the cut: real keys of the band experts in double-double
+      DD kd[MAXJ];
+#pragma unroll 1
+      for (int j = 0; j < MAXJ; ++j) {
+        kd[j] = DD{0.0, 0.0};
+        const bool mine = (band >> j) & 1u;
+        if (__any_sync(FULL_MASK, mine) && mine) kd[j] = dd_sigmoid_key(u[j], b[j]);
+      }
+      picked = 0;
+      for (int r = 0; r < need; ++r) {
+        // this lane's best remaining band expert (lowest index among real ties), then the warp's
+        DD v = {0.0, 0.0};
+        int i = -1;
+#pragma unroll 1
+        for (int j = 0; j < MAXJ; ++j)
+          if (((band & ~picked) >> j) & 1u)
+            if (i < 0 || dd_cmp(kd[j], v) < 0) { v = kd[j]; i = j * 32 + lane; }
+        warp_argmax_dd(v, i, i >= 0);
+        if (i < 0) return false;
+#pragma unroll 1
+        for (int j = 0; j < MAXJ; ++j)
+          if (i == j * 32 + lane) picked |= 1u << j;
+      }
     }
   }
   // lane r < K takes the r-th chosen expert (any order: the caller sorts them)
@@ -633,8 +737,9 @@ __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
       // (the n-th largest of perturbed values moves by at most the largest perturbation) plus
       // the rounding of the sum.
       kmax = warp_max(kmax);
-      const float gtol = a.topn * key_tol(kmax) + 6e-8f * fabsf(sel.gkth);
-      redo = (double)sel.kth - (double)sel.next <= 2.0 * key_tol(sel.kth) ||
+      const float tol = key_tol(kmax, sigmoid);  // every key's error, whatever its size
+      const float gtol = a.topn * tol + 6e-8f * fabsf(sel.gkth);
+      redo = (double)sel.kth - (double)sel.next <= 2.0 * tol ||
              (a.G > a.Gk && (double)sel.gkth - (double)sel.gnext <= 2.0 * gtol);
     }
     int sel_e = sel.e;

@@ -14,7 +14,11 @@ from tests.helpers import MID_A, MID_B, MID_ODD, MID_V2, rel_frob, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
-CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_odd": MID_ODD}
+CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_odd": MID_ODD,
+        # batches of at most 64 and 128 tokens run the expert GEMMs with the 64- and 128-token
+        # ring geometries (more stages of fewer token rows)
+        "mid_a_t50": MID_A.replace(name="mid_a_t50", T=50),
+        "mid_odd_t100": MID_ODD.replace(name="mid_odd_t100", T=100)}
 
 
 def _perm_inputs(cfg, seed=3):
@@ -33,8 +37,9 @@ def _expert_of_rows(offs):
     return np.repeat(np.arange(len(offs) - 1), np.diff(offs))
 
 
-@pytest.mark.parametrize("name", ["tiny", "mid_a", "mid_b", "mid_v2", "mid_odd", "v1", "v2",
-                                  "v3_prefill", "v3_decode_32", "v3_decode_512"])
+@pytest.mark.parametrize("name", ["tiny", "mid_a", "mid_b", "mid_v2", "mid_odd", "mid_a_t50",
+                                  "mid_odd_t100", "v1", "v2", "v3_prefill", "v3_decode_32",
+                                  "v3_decode_128", "v3_decode_512"])
 def test_expert_ffn(name):
     import mixture_experts_routing_sigmoid_b300 as moe
     cfg = CFGS[name]
@@ -120,7 +125,7 @@ def test_combine(name):
         assert np.all(np.abs(got - want) <= 2 ** -8 * np.abs(want) + 1e-2)
 
 
-@pytest.mark.parametrize("name", ["mid_a", "v3_prefill_e32"])
+@pytest.mark.parametrize("name", ["mid_a", "mid_a_t50", "mid_odd_t100", "v3_prefill_e32"])
 def test_tile_schedule_does_not_change_results(name):
     """moe_expert_ffn (workspace given: tiles claimed dynamically from a counter) and
     moe_expert_up + moe_expert_down (no workspace: static round-robin tiles) compute every output
@@ -151,8 +156,8 @@ def test_tile_schedule_does_not_change_results(name):
     assert torch.equal(ys_dyn, ys_st)
 
 
-@pytest.mark.parametrize("name", ["mid_a", "mid_odd", "mid_v2", "v3_decode_32", "v3_decode_512",
-                                  "v3_prefill_e32", "v1"])
+@pytest.mark.parametrize("name", ["mid_a", "mid_odd", "mid_v2", "mid_a_t50", "mid_odd_t100",
+                                  "v3_decode_32", "v3_decode_512", "v3_prefill_e32", "v1"])
 def test_row_gather_equals_permuted_copy(name):
     """The up projection reading its routed rows from x through row_token (tile::gather4 loads,
     what moe_layer_forward runs) gives bitwise the outputs of the same GEMM on the permuted copy

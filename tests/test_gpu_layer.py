@@ -110,7 +110,7 @@ def test_layer_full_size_sampled(name, n_sample):
     _run(CFGS[name], n_sample)
 
 
-@pytest.mark.parametrize("T", [1, 2, 129])
+@pytest.mark.parametrize("T", [1, 2, 33, 64, 65, 128, 129])
 def test_layer_odd_token_counts(T):
     _run(MID_A.replace(T=T), T)
     _run(CONFIGS["v3_decode_32"].replace(T=T), min(T, 8))

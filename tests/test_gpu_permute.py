@@ -108,3 +108,22 @@ def test_permute_single_block_boundaries(T):
     cfg = MID_A.replace(T=T)
     idx, w = _oracle_routing(cfg, T)
     _check(cfg, T, idx, w, with_x=True)
+
+
+@pytest.mark.parametrize("per_dev0", [2, 4])
+def test_drop_device_with_more_keys_than_shared_memory(per_dev0):
+    """The drop's radix select keeps up to 20480 keys of a device in shared memory and streams
+    them from global memory beyond that: a v2-sized batch (T = 8192, K = 6) putting 2 of each
+    token's 6 slots on device 0 (16384 keys: shared memory) or 4 (32768 keys: streamed), with
+    random weights and ties, drops bit-exactly as the oracle does."""
+    cfg = CONFIGS["v2"]
+    T, K, N, G = cfg.T, cfg.top_k, cfg.n_routed, cfg.n_groups
+    per = N // G
+    rng = np.random.default_rng(per_dev0)
+    idx = np.empty((T, K), np.int32)
+    for t in range(T):
+        dev0 = rng.choice(per, size=per_dev0, replace=False)
+        rest = rng.choice(np.arange(per, N), size=K - per_dev0, replace=False)
+        idx[t] = np.sort(np.concatenate([dev0, rest]))
+    w = np.round(rng.random((T, K)) * 64) / 64  # many exact ties
+    _check(cfg, T, idx, w, with_x=False)
