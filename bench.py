@@ -38,6 +38,8 @@ def parse():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--config", default="v3_prefill")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the config's batch size T (profiling cases)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -217,6 +219,14 @@ def traffic_per_launch(workload: str):
     return float(c["dram_read_bytes"] + c["dram_write_bytes"]) * float(c.get("scale_to", 1.0))
 
 
+def config_of(args):
+    from moe_inputs import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.tokens is not None:
+        cfg = cfg.replace(name=f"{cfg.name}_t{args.tokens}", T=args.tokens)
+    return cfg
+
+
 def workload_name(cfg) -> str:
     return (f"{cfg.name}: T={cfg.T} H={cfg.hidden} N={cfg.n_routed} G={cfg.n_groups} "
             f"Gk={cfg.topk_groups} K={cfg.top_k} S={cfg.n_shared} I={cfg.inter} "
@@ -233,7 +243,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = CONFIGS[args.config]
+    cfg = config_of(args)
     T, H, K, N = cfg.T, cfg.hidden, cfg.top_k, cfg.n_routed
     w = make_weights(cfg, device=dev, seed=0)
     x = make_x(cfg, device=dev, seed=0)
@@ -514,7 +524,7 @@ def run_reference(args, world, rank, local):
     """The oracle, as it stands, on the host cores: same metric / unit / config as our arm."""
     import torch
     from moe_inputs import CONFIGS, make_weights, make_x
-    cfg = CONFIGS[args.config]
+    cfg = config_of(args)
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     w = make_weights(cfg, device=dev, seed=0)
     x = make_x(cfg, device=dev, seed=0)

@@ -102,7 +102,7 @@ constexpr int32_t kGatherMaxTokens = 32;
 
 // Workspace carve for one config and token count. Every region is 256-byte aligned.
 struct Layout {
-  size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_lse,
+  size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_c, part_lse,
       counts, recv, seq_s, seq_c, seq_lb, gate_part, sched, xy_perm, h, h_sh, y_sh, total;
 };
 
@@ -127,6 +127,7 @@ Layout layout(const moe_config* c, int32_t T) {
   L.base = take(nb * N * 4);
   L.thr = take((size_t)c->n_groups * 8);
   L.part_s = take(nbs * N * 4);
+  L.part_c = take(nbs * N * 4);
   L.part_lse = take(nbs * 2 * 8);
   L.counts = take(N * 4);
   L.recv = take(32 * 4);
@@ -250,7 +251,8 @@ moe_status do_stats(const moe_config* c, int32_t T, const float* u, const int32_
   s.counts = counts ? counts : at<int32_t>(ws, L.counts);
   s.f = f; s.P = P; s.lb_z = lb_z;
   s.part_s = at<float>(ws, L.part_s);
-  s.part_lse = at<double>(ws, L.part_lse);
+  s.part_c = at<int32_t>(ws, L.part_c);
+  s.part_lse = at<float>(ws, L.part_lse);
   s.nblk = stats_blocks(T);
   s.err = error_word();
   return cuda_status(launch_stats(s, st), "load stats");
@@ -652,7 +654,8 @@ moe_status moe_group_balance_losses(const moe_config* cfg, int32_t T, const floa
   a.st.counts = at<int32_t>(ws, L.counts);
   a.st.f = nullptr; a.st.P = nullptr; a.st.lb_z = nullptr;
   a.st.part_s = at<float>(ws, L.part_s);
-  a.st.part_lse = at<double>(ws, L.part_lse);
+  a.st.part_c = nullptr;  // the device-loss kernels count on their own
+  a.st.part_lse = at<float>(ws, L.part_lse);
   a.st.nblk = stats_blocks(T);
   a.st.err = error_word();
   a.G = cfg->n_groups;

@@ -320,6 +320,46 @@ __device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const void* tmap,
          "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
+// ------------------------------------------------------------------ L2 residency hints
+// Policies for the .L2::cache_hint forms below: lines loaded or stored with evict_first go
+// first when L2 needs room, evict_last ones last (a hint; it changes no result).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// tma_load_2d_pair / tma_load_5d_pair with an L2 policy for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* tmap,
+                                                      uint32_t bar_cluster, int c0, int c1,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1),
+         "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair_hint(uint32_t dst, const void* tmap,
+                                                      uint32_t bar_cluster, int c0, int c1,
+                                                      int c2, int c3, int c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1),
+         "r"(c2), "r"(c3), "r"(c4), "l"(policy)
+      : "memory");
+}
+// 32-bit global store with an L2 policy.
+__device__ __forceinline__ void st_u32_hint(void* p, uint32_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" :: "l"(p), "r"(v), "l"(policy)
+               : "memory");
+}
+
 // TMEM allocation shared by the CTA pair: one warp of EACH CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t holder, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"

@@ -51,7 +51,8 @@ struct StatsArgs {
   float* P;             // [N] or nullptr
   float* lb_z;          // [3] or nullptr
   float* part_s;        // scratch [nblk, N]
-  double* part_lse;     // scratch [nblk, 2]
+  int32_t* part_c;      // scratch [nblk, N] assignment counts, or nullptr (counts are given)
+  float* part_lse;      // scratch [nblk, 2]
   int nblk;
   int* err;
 };

@@ -222,36 +222,47 @@ __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
   }
 }
 
-// Batches of at most SB_MAX_T tokens: histogram, scan and scatter in one CTA (one thread per
-// token, at least one per expert), the same arithmetic as the three kernels above with the
-// bitmasks ([N][W] words, W = ceil(T / 32)) in shared memory.
+// Batches of at most SB_MAX_T tokens: one kernel, SB_CTAS CTAs of one thread per token (at least
+// one per expert). Every CTA counts the kept assignments of all experts in shared memory and scans
+// the counts (so every CTA knows every segment's offset), then places the assignments of its own
+// experts (experts cta * epb .. + epb - 1): a token's rank inside its expert is the number of
+// earlier tokens in that expert's bitmask ([epb][W] words, W = ceil(T / 32)). Same arithmetic as
+// the three-kernel path above; the work is spread so that no CTA walks a long serial chain.
 constexpr int SB_MAX_T = 1024;
-__global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs p) {
+constexpr int SB_CTAS = 32;
+__global__ void __launch_bounds__(SB_MAX_T) perm_small_kernel(PermuteArgs p) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ uint32_t sm[];  // [N][W] masks, then [N + 1] exclusive offsets
+  extern __shared__ uint32_t sm[];  // [epb][W] masks, [N] counts, [N + 1] exclusive offsets
+  __shared__ int wsum[SB_MAX_T / 32];
   const int W = (p.T + 31) >> 5;
-  int* excl = reinterpret_cast<int*>(sm + p.N * W);
-  for (int i = threadIdx.x; i < p.N * W; i += blockDim.x) sm[i] = 0;
+  const int epb = (p.N + gridDim.x - 1) / gridDim.x;
+  const int e0 = blockIdx.x * epb;
+  int* cnt = reinterpret_cast<int*>(sm + epb * W);
+  int* excl = cnt + p.N;
+  for (int i = threadIdx.x; i < epb * W; i += blockDim.x) sm[i] = 0;
+  for (int i = threadIdx.x; i < p.N; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
   const int t = threadIdx.x;
   if (t < p.T) {
     for (int k = 0; k < p.K; ++k) {
       const long long a = (long long)t * p.K + k;
       const int e = p.idx[a];
-      if (e < 0 || e >= p.N) { set_error(p.err, ERR_DEVICE_CHECK); continue; }
-      if (is_kept(p, a, e)) atomicOr(&sm[e * W + (t >> 5)], 1u << (t & 31));
+      if (e < 0 || e >= p.N) {
+        if (blockIdx.x == 0) set_error(p.err, ERR_DEVICE_CHECK);
+        continue;
+      }
+      if (!is_kept(p, a, e)) continue;
+      atomicAdd(&cnt[e], 1);
+      if (e >= e0 && e < e0 + epb) atomicOr(&sm[(e - e0) * W + (t >> 5)], 1u << (t & 31));
     }
   }
   __syncthreads();
   {
     // exclusive scan of the per-expert counts (N <= blockDim): warp scans, then warp totals
-    __shared__ int wsum[SB_MAX_T / 32];
     const int e = threadIdx.x, lane = e & 31, wi = e >> 5;
-    int cnt = 0;
-    if (e < p.N)
-      for (int w = 0; w < W; ++w) cnt += __popc(sm[e * W + w]);
-    int incl = cnt;
+    const int c = e < p.N ? cnt[e] : 0;
+    int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(FULL_MASK, incl, o);
@@ -261,15 +272,13 @@ __global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs
     __syncthreads();
     int before = 0;
     for (int i = 0; i < wi; ++i) before += wsum[i];
-    if (e < p.N) {
-      excl[e] = before + incl - cnt;
-      p.offsets[e] = before + incl - cnt;
+    if (e < p.N) excl[e] = before + incl - c;
+    if (e == p.N - 1) excl[p.N] = before + incl;
+    if (blockIdx.x == 0) {
+      if (e < p.N) p.offsets[e] = before + incl - c;
+      if (e == p.N - 1) p.offsets[p.N] = before + incl;
+      if (e == 0 && p.sched_zero != nullptr) { p.sched_zero[0] = 0; p.sched_zero[1] = 0; }
     }
-    if (e == p.N - 1) {
-      excl[p.N] = before + incl;
-      p.offsets[p.N] = before + incl;
-    }
-    if (e == 0 && p.sched_zero != nullptr) { p.sched_zero[0] = 0; p.sched_zero[1] = 0; }
   }
   __syncthreads();
   if (t < p.T) {
@@ -278,8 +287,13 @@ __global__ void __launch_bounds__(SB_MAX_T) perm_single_block_kernel(PermuteArgs
     for (int k = 0; k < p.K; ++k) {
       const long long a = (long long)t * p.K + k;
       const int e = p.idx[a];
-      if (e < 0 || e >= p.N || !is_kept(p, a, e)) { p.slot_row[a] = -1; continue; }
-      const uint32_t* m = sm + e * W;
+      if (e < 0 || e >= p.N) {
+        if (blockIdx.x == 0) p.slot_row[a] = -1;
+        continue;
+      }
+      if (e < e0 || e >= e0 + epb) continue;  // another CTA's expert
+      if (!is_kept(p, a, e)) { p.slot_row[a] = -1; continue; }
+      const uint32_t* m = sm + (e - e0) * W;
       int rank = __popc(m[wi] & below);
       for (int i = 0; i < wi; ++i) rank += __popc(m[i]);
       const int row = excl[e] + rank;
@@ -347,8 +361,10 @@ cudaError_t launch_permute(const PermuteArgs& p, int num_sms, cudaStream_t st) {
     const int W = (p.T + 31) / 32;
     int threads = ((p.T + 31) / 32) * 32;
     if (threads < p.N) threads = ((p.N + 31) / 32) * 32;
-    return launch_pdl(perm_single_block_kernel, dim3(1), dim3(threads),
-                      (p.N * W + p.N + 1) * sizeof(uint32_t), st, p);
+    const int ctas = p.N < SB_CTAS ? p.N : SB_CTAS;
+    const int epb = (p.N + ctas - 1) / ctas;
+    return launch_pdl(perm_small_kernel, dim3(ctas), dim3(threads),
+                      (size_t)(epb * W + 2 * p.N + 1) * sizeof(uint32_t), st, p);
   }
   cudaError_t e = launch_pdl(perm_hist_kernel, dim3(nb), dim3(PB), p.N * 8 * sizeof(uint32_t), st, p);
   if (e == cudaSuccess) e = launch_pdl(perm_scan_kernel, dim3(1), dim3(256), 0, st, p, nb);

@@ -814,19 +814,40 @@ __global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
 }
 
 // ---------------------------------------------------------------- load statistics
-// Per-block partial sums of the scores of every expert and of lse, lse^2 over its tokens.
-__global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
+// All in fp32: this part's fp64 throughput is a small fraction of its fp32 rate, and a reduction
+// on one SM in fp64 cost more than the rest of the statistics together. Long sums are
+// compensated (Kahan) and every sum has a fixed order, so the results are deterministic and far
+// inside the 1e-5 relative accuracy the statistics are held to.
+struct Kahan {
+  float s = 0.0f, c = 0.0f;
+  __device__ __forceinline__ void add(float v) {
+    const float y = v - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+};
+
+// Per-block partial sums over the block's tokens (one warp per token, STATS_TOK_PER_WARP tokens
+// each): the scores of every expert, lse and lse^2, and (with part_c) the assignment counts.
+constexpr int STATS_TOK_PER_WARP = 2;
+constexpr int STATS_THREADS = 256;
+__global__ void __launch_bounds__(STATS_THREADS) stats_partial_kernel(StatsArgs a) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[8][256];
-  __shared__ double redl[8][2];
+  __shared__ float redl[8][2];
+  __shared__ int cnt[256];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int J = (a.N + 31) >> 5;
   const int warps = (gridDim.x * blockDim.x) >> 5;
+  if (a.part_c != nullptr)
+    for (int e = threadIdx.x; e < 256; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
   float acc[MAXJ];
 #pragma unroll
   for (int j = 0; j < MAXJ; ++j) acc[j] = 0.0f;
-  double l1 = 0.0, l2 = 0.0;
+  float l1 = 0.0f, l2 = 0.0f;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < a.T; t += warps) {
     const float* ut = a.u + (size_t)t * a.N;
     float u[MAXJ];
@@ -834,6 +855,11 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
     for (int j = 0; j < MAXJ; ++j) {
       const int e = j * 32 + lane;
       u[j] = (j < J && e < a.N) ? ut[e] : -INFINITY;
+    }
+    if (a.part_c != nullptr && lane < a.K) {
+      const int e = a.idx[(size_t)t * a.K + lane];
+      if (e >= 0 && e < a.N) atomicAdd(&cnt[e], 1);
+      else set_error(a.err, ERR_DEVICE_CHECK);
     }
     float m = u[0];
 #pragma unroll
@@ -851,7 +877,7 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
 #pragma unroll
       for (int j = 0; j < MAXJ; ++j) acc[j] += ex[j] / z;
     }
-    const double lse = (double)m + log((double)z);
+    const float lse = m + logf(z);
     l1 += lse;
     l2 += lse * lse;
   }
@@ -866,64 +892,99 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
     float s = 0.0f;
     for (int w = 0; w < 8; ++w) s += red[w][e];
     a.part_s[(size_t)blockIdx.x * a.N + e] = s;
+    if (a.part_c != nullptr) a.part_c[(size_t)blockIdx.x * a.N + e] = cnt[e];
   }
   if (threadIdx.x == 0) {
-    double s1 = 0.0, s2 = 0.0;
+    float s1 = 0.0f, s2 = 0.0f;
     for (int w = 0; w < 8; ++w) { s1 += redl[w][0]; s2 += redl[w][1]; }
     a.part_lse[blockIdx.x * 2 + 0] = s1;
     a.part_lse[blockIdx.x * 2 + 1] = s2;
   }
 }
 
-__global__ void stats_count_kernel(const int32_t* idx, long long n, int N, int32_t* counts,
-                                   int* err) {
-  pdl_wait();
-  pdl_trigger();
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int e = idx[i];
-    if (e >= 0 && e < N) atomicAdd(&counts[e], 1);
-    else set_error(err, ERR_DEVICE_CHECK);
+// Tree sum over the 1024 threads of a block in a fixed order (every thread gets the result).
+__device__ __forceinline__ float block_sum_1024(float v, float* sh) {
+  sh[threadIdx.x] = v;
+  __syncthreads();
+  for (int o = 512; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
   }
+  const float r = sh[0];
+  __syncthreads();
+  return r;
 }
 
-// Fixed-order fp64 reduction of the partials: f, P, L_B, L_Z, mean lse.
-__global__ void __launch_bounds__(256) stats_final_kernel(StatsArgs a) {
+// Fixed-order reduction of the partials: counts, f, P, L_B, L_Z, mean lse. Q = 1024 / N' threads
+// share each expert's column of partials (N' = N rounded up to a power of two): thread (q, e)
+// sums blocks q, q + Q, ... (compensated, eight loads in flight), then the Q sums of a column are
+// added in the order q = 0 .. Q-1.
+constexpr int STATS_FINAL_THREADS = 1024;
+__global__ void __launch_bounds__(STATS_FINAL_THREADS) stats_final_kernel(StatsArgs a) {
   pdl_wait();
   pdl_trigger();
-  __shared__ double colsum[256];
-  __shared__ double term[256];
-  const int e = threadIdx.x;
-  double cs = 0.0;
-  if (e < a.N)
-    for (int b = 0; b < a.nblk; ++b) cs += (double)a.part_s[(size_t)b * a.N + e];
-  colsum[e] = cs;
-  __syncthreads();
-  if (e == 0) {
-    double tot = 0.0;
-    for (int i = 0; i < a.N; ++i) tot += colsum[i];
-    term[0] = tot;
-  }
-  __syncthreads();
-  const double total = term[0];
-  __syncthreads();
-  double fe = 0.0, pe = 0.0;
+  __shared__ float tree[STATS_FINAL_THREADS];
+  __shared__ int ctree[STATS_FINAL_THREADS];
+  int np2 = 1;
+  while (np2 < a.N) np2 <<= 1;
+  const int Q = STATS_FINAL_THREADS / np2;
+  const int e = threadIdx.x % np2, q = threadIdx.x / np2;
+  Kahan cs;
+  int cc = 0;
   if (e < a.N) {
-    fe = (double)a.counts[e] / ((double)a.T * a.K);
-    pe = colsum[e] / total;
-    if (a.f) a.f[e] = (float)fe;
-    if (a.P) a.P[e] = (float)pe;
+    for (int b0 = q; b0 < a.nblk; b0 += 8 * Q) {
+      float v[8];
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int b = b0 + Q * j;
+        v[j] = b < a.nblk ? a.part_s[(size_t)b * a.N + e] : 0.0f;
+        c[j] = (b < a.nblk && a.part_c != nullptr) ? a.part_c[(size_t)b * a.N + e] : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cs.add(v[j]);
+        cc += c[j];
+      }
+    }
   }
-  term[e] = (e < a.N) ? fe * pe : 0.0;
+  // lse sums: blocks strided over the threads (compensated), then a tree
+  Kahan s1, s2;
+  for (int b = threadIdx.x; b < a.nblk; b += STATS_FINAL_THREADS) {
+    s1.add(a.part_lse[2 * b]);
+    s2.add(a.part_lse[2 * b + 1]);
+  }
+  tree[threadIdx.x] = cs.s;
+  ctree[threadIdx.x] = cc;
   __syncthreads();
-  if (e == 0 && a.lb_z) {
-    double lb = 0.0;
-    for (int i = 0; i < a.N; ++i) lb += term[i];
-    double s1 = 0.0, s2 = 0.0;
-    for (int b = 0; b < a.nblk; ++b) { s1 += a.part_lse[2 * b]; s2 += a.part_lse[2 * b + 1]; }
-    a.lb_z[0] = (float)(lb * a.N);
-    a.lb_z[1] = (float)(s2 / a.T);
-    a.lb_z[2] = (float)(s1 / a.T);
+  float colsum = 0.0f;
+  int count = 0;
+  if (q == 0 && e < a.N) {
+    Kahan col;
+    for (int i = 0; i < Q; ++i) {
+      col.add(tree[i * np2 + e]);
+      count += ctree[i * np2 + e];
+    }
+    colsum = col.s;
+    if (a.part_c == nullptr) count = a.counts[e];
+  }
+  __syncthreads();
+  const float total = block_sum_1024(q == 0 ? colsum : 0.0f, tree);
+  float fe = 0.0f, pe = 0.0f;
+  if (q == 0 && e < a.N) {
+    if (a.part_c != nullptr) a.counts[e] = count;
+    fe = (float)count / ((float)a.T * (float)a.K);
+    pe = colsum / total;
+    if (a.f) a.f[e] = fe;
+    if (a.P) a.P[e] = pe;
+  }
+  const float lb = block_sum_1024(fe * pe, tree);
+  const float l1 = block_sum_1024(s1.s, tree);
+  const float l2 = block_sum_1024(s2.s, tree);
+  if (threadIdx.x == 0 && a.lb_z) {
+    a.lb_z[0] = lb * a.N;
+    a.lb_z[1] = l2 / a.T;
+    a.lb_z[2] = l1 / a.T;
   }
 }
 
@@ -1010,7 +1071,7 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
 }
 
 int stats_blocks(int T) {
-  int b = (T + 63) / 64;  // 8 warps x 8 tokens
+  int b = (T + 8 * STATS_TOK_PER_WARP - 1) / (8 * STATS_TOK_PER_WARP);  // 8 warps per block
   if (b < 1) b = 1;
   if (b > 1184) b = 1184;
   return b;
@@ -1018,14 +1079,9 @@ int stats_blocks(int T) {
 
 cudaError_t launch_stats(const StatsArgs& a, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(a.counts, 0, sizeof(int32_t) * a.N, st);
-  if (e != cudaSuccess) return e;
-  const long long n = (long long)a.T * a.K;
-  int cb = (int)((n + 255) / 256);
-  if (cb > 1184) cb = 1184;
-  e = launch_pdl(stats_count_kernel, dim3(cb), dim3(256), 0, st, a.idx, n, a.N, a.counts, a.err);
-  if (e == cudaSuccess) e = launch_pdl(stats_partial_kernel, dim3(a.nblk), dim3(256), 0, st, a);
-  if (e == cudaSuccess) e = launch_pdl(stats_final_kernel, dim3(1), dim3(256), 0, st, a);
+  cudaError_t e = launch_pdl(stats_partial_kernel, dim3(a.nblk), dim3(STATS_THREADS), 0, st, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(stats_final_kernel, dim3(1), dim3(STATS_FINAL_THREADS), 0, st, a);
   return e;
 }
 
