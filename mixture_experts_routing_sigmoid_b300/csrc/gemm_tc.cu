@@ -29,7 +29,7 @@
 // each store instruction covering a contiguous run of one token's output row (neighbouring
 // lanes swap values to write bf16 pairs). No shared-memory staging.
 //
-// Persistent kernel, one 224-thread CTA per SM. Tiles are numbered problem by problem (most
+// Persistent kernel, one 352-thread CTA per SM. Tiles are numbered problem by problem (most
 // rows first), weight tile by weight tile, token tile fastest (a segment's rows are split into
 // equal token tiles). The first wave is one tile per CTA pair; after that a pair claims the next
 // index from a counter when its producer starts the current tile (round robin without a
@@ -44,9 +44,12 @@
 //   warp 1      TMEM owner (both CTAs) and, in the first CTA, MMA issuer: a single thread waits
 //               for each stage and issues its tcgen05.mma (M=256, N=tile's tokens rounded up to
 //               16, K=16; four per unit) into one of two 256-column fp32 accumulators.
-//   warps 2..5  epilogue (both CTAs): tcgen05.ld of the warp's 32 TMEM lanes, SwiGLU / router
-//               bias, stores.
-//   warp 6      tile scheduler: in the first CTA it claims, decodes and publishes each tile in
+//   warps 2..9  epilogue (both CTAs): two warps per quarter of the TMEM lanes (a warp may only
+//               read its own quarter), taking alternate 32-column chunks: tcgen05.ld, SwiGLU /
+//               router bias, stores. Two warps per quarter keep a short tile's epilogue (a few
+//               k blocks, as with the small intermediate sizes) shorter than the next tile's
+//               main loop.
+//   warp 10     tile scheduler: in the first CTA it claims, decodes and publishes each tile in
 //               the CTA's local ring and sends it to the second CTA by st.async; in the second
 //               CTA it relays the received tiles into that CTA's local ring.
 // Token columns past the segment end belong to the next expert (or lie beyond the tensor,
@@ -66,7 +69,9 @@ constexpr int BM = 128;                  // weight rows per CTA and operand (MMA
 constexpr int KU = 64;                   // reduction elements per unit (128 bytes of bf16)
 constexpr int UNITS = 2;                 // units per stage (k block of 128 elements)
 constexpr int MAXP = 258;
-constexpr int THREADS = 224;
+constexpr int THREADS = 352;
+constexpr int EPI_WARPS = 8;             // warps 2 .. 9
+constexpr int SCHED_WARP = 10;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;       // two accumulators
 constexpr int XBOX_S = 32, XBOX_L = 64;  // token rows per TMA box (small / large map)
@@ -140,7 +145,7 @@ struct SmemCtl {
   uint64_t full[MAX_STAGES];   // first CTA's copy counts both CTAs' loads
   uint64_t empty[MAX_STAGES];  // per CTA, arrived on by the MMA commit
   uint64_t tfull[2];           // per CTA, arrived on by the MMA commit
-  uint64_t tempty[2];          // first CTA's copy: 4 epilogue warps x 2 CTAs
+  uint64_t tempty[2];          // first CTA's copy: every epilogue warp of both CTAs
   uint64_t drain;
   // tile schedule: a CTA-local ring in each CTA (written by the CTA's producer, read by its
   // MMA issuer and epilogue warps) and a channel from the first CTA's producer to the second's
@@ -330,8 +335,8 @@ __device__ __forceinline__ void store_bf16_chunk(const float (&v)[NT], __nv_bflo
 // republishes it in its own local ring. The producer, MMA issuer and epilogue warps only read
 // their local ring: no wait on their path is cluster-scope, and no decoding sits between two
 // stages of a producer or MMA issuer.
-constexpr uint32_t LOCAL_READERS_0 = 6;  // first CTA: producer, MMA issuer, 4 epilogue warps
-constexpr uint32_t LOCAL_READERS_1 = 5;  // second CTA: producer, 4 epilogue warps
+constexpr uint32_t LOCAL_READERS_0 = 2 + EPI_WARPS;  // first CTA: producer, MMA issuer, epilogue
+constexpr uint32_t LOCAL_READERS_1 = 1 + EPI_WARPS;  // second CTA: producer, epilogue
 constexpr uint32_t TILE_BYTES = sizeof(Tile);
 
 __device__ __forceinline__ void sts_tile(uint32_t a, const Tile& t) {
@@ -463,7 +468,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(bar(c.full[s]), 1); mbar_init(bar(c.empty[s]), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(bar(c.tfull[a]), 1); mbar_init(bar(c.tempty[a]), 8); }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(c.tfull[a]), 1);
+      mbar_init(bar(c.tempty[a]), 2 * EPI_WARPS);  // every epilogue warp of both CTAs
+    }
     mbar_init(bar(c.drain), 1);
     for (int s = 0; s < SQ; ++s) {
       mbar_init(bar(c.lfull[s]), 1);
@@ -713,7 +721,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         grace_wait(bar(c.drain), 0);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == SCHED_WARP) {
     // ================================================================ tile scheduler
     // First CTA: tiles one per pair in pair order first; then either round robin (static) or,
     // with a tile counter, in index order to whichever pair asks next: a pair claims its next
@@ -747,6 +755,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   } else {
     // ================================================================ epilogue
     const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;        // chunks ch with ch % 2 == h
     const bool hint = p.l2_hints != 0;
     const uint64_t pol_o = l2_policy_evict_last();
     const uint32_t tempty0 = mapa_shared(bar(c.tempty[0]), 0);
@@ -762,14 +771,19 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
       const int fc = t.f0 + (int)rank * feat_per_cta<MODE>();  // this CTA's first feature
       const int nch = (t.nrows + 31) / 32;
-      for (int ch = 0; ch < nch; ++ch) {
+      if (h >= nch) {
+        // no chunk of this tile for this warp: the accumulator is free as far as it goes
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
+      }
+      for (int ch = h; ch < nch; ch += 2) {
         const int nvalid = t.nrows - ch * 32;
         const size_t row0 = (size_t)(t.r0 + ch * 32);
         uint32_t v[32];
         tmem_ld_32cols(tb + ch * 32, v);
         tmem_wait_ld_fence(v);
-        if (ch == nch - 1) {
-          // accumulator fully read: hand it back to the MMA issuer before the stores
+        if (ch + 2 >= nch) {
+          // this warp's share of the accumulator read: hand it back before the stores
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
