@@ -86,6 +86,16 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ instruction placement
+// An empty volatile statement that reads v: the compiler computes v before it, and volatile
+// statements keep their order, so placed before an mbarrier wait it keeps the work that v needs
+// off the path from the barrier's release to the instructions that follow the wait.
+__device__ __forceinline__ void ready_before(uint32_t v) { asm volatile("" :: "r"(v)); }
+__device__ __forceinline__ void ready_before(uint64_t v) { asm volatile("" :: "l"(v)); }
+__device__ __forceinline__ void ready_before(const void* v) {
+  asm volatile("" :: "l"(reinterpret_cast<uint64_t>(v)));
+}
+
 // ------------------------------------------------------------------ timers, shared memory
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;

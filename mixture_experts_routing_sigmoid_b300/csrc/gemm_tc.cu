@@ -35,10 +35,10 @@
 // index from a counter when its producer starts the current tile (round robin without a
 // counter), so the pairs sharing a weight tile run it together and its second read hits L2.
 //   warp 0      TMA producer (both CTAs): this CTA's weight rows and token rows of one k block
-//               per stage, 3-stage ring of 64 KB stages. A k block is 128 elements, two
-//               128-byte-swizzled units of 64 (one TMA box per operand and unit); when K / 64 is
-//               odd the last block holds one unit. Fewer, larger stages halve the barrier
-//               round trips per FLOP at the same bytes in flight.
+//               per stage, in a 200 KB ring of stages sized by the tile (below). A k block is
+//               128 elements, two 128-byte-swizzled units of 64 (one TMA box per operand and
+//               unit); when K / 64 is odd the last block holds one unit. Two units per stage
+//               halve the barrier round trips per FLOP against one-unit stages.
 //               Completion of both CTAs' loads is counted on the first CTA's full barrier; the
 //               MMA's commit frees the stage in both CTAs.
 //   warp 1      TMEM owner (both CTAs) and, in the first CTA, MMA issuer: a single thread waits
@@ -84,22 +84,21 @@ constexpr int kL2HintMaxTokens = 128;    // batches whose expert GEMMs use the L
 constexpr int A_UNIT = BM * KU * 2;      // this CTA's weight rows, one unit
 constexpr int A_BYTES = UNITS * A_UNIT;
 
-// Ring geometry: tokens per tile at most (MMA N) and ring stages. A stage holds a k block of
-// the CTA's weight rows (32 KB) and of its half of the tile's tokens (TOK/2 rows). Fewer tokens
-// per tile leave room for more stages, i.e. more weight bytes in flight per CTA, which is what a
-// tile with few tokens (a weight stream) needs; a tile with many tokens needs the wide MMA.
-//   GEO 0: 256 tokens, 3 stages of 64 KB (any batch; the only one the router GEMM uses)
-//   GEO 1: 128 tokens, 4 stages of 48 KB (batches of at most 128 tokens: one tile per expert)
-//   GEO 2:  64 tokens, 5 stages of 40 KB (batches of at most 64 tokens)
-template <int GEO> struct Geom;
-template <> struct Geom<0> { static constexpr int TOK = 256, STAGES = 3; };
-template <> struct Geom<1> { static constexpr int TOK = 128, STAGES = 4; };
-template <> struct Geom<2> { static constexpr int TOK = 64, STAGES = 5; };
-constexpr int MAX_STAGES = 5, MAX_TOK = 256;
-template <int GEO>  // this CTA's token rows (at most), one unit
-__host__ __device__ constexpr int b_unit() { return Geom<GEO>::TOK / 2 * KU * 2; }
-template <int GEO>
-__host__ __device__ constexpr int stage_bytes() { return A_BYTES + UNITS * b_unit<GEO>(); }
+// Operand ring: RING_BYTES of shared memory cut into stages whose size follows the tile. A
+// stage holds a k block of the CTA's 128 weight rows (32 KB) and of its half of the tile's
+// tokens, so a tile with few tokens takes small stages and keeps more of them in flight:
+// 256 tokens, 3 stages of 64 KB; 128 tokens, 4 of 48 KB; 64 or fewer, 5 of 34-40 KB. A tile
+// with few tokens streams its weights and needs bytes in flight; a tile with many tokens needs
+// the wide MMA; in a skewed batch both kinds run side by side in one launch, each at its depth.
+// Stages are placed one after the other and wrap to the start of the ring when the next one
+// does not fit; NS barrier pairs are used in turn, which also bounds the stages in flight.
+// Launches whose tiles all stream many tokens (large batches) use NS = 3 (measured: rotating
+// six slots there costs 1-2%); batches of at most kDeepRingMaxTokens tokens, where most
+// tiles stream weights, use NS = NSLOT.
+constexpr int TOK = 256;                 // tokens per tile at most (MMA N)
+constexpr uint32_t RING_BYTES = 200 * 1024;
+constexpr int NSLOT = 6;                 // more than the stages that fit at once
+constexpr int kDeepRingMaxTokens = 512;
 
 struct TcParams {
   CUtensorMap tmW0, tmW1;    // weights: routed, shared (box 128 rows; UP: interleaved 5-D box)
@@ -142,8 +141,8 @@ constexpr int TILE_WORDS = sizeof(Tile) / 4;
 static_assert(TILE_WORDS == 12, "a tile travels as three 16-byte vectors");
 
 struct SmemCtl {
-  uint64_t full[MAX_STAGES];   // first CTA's copy counts both CTAs' loads
-  uint64_t empty[MAX_STAGES];  // per CTA, arrived on by the MMA commit
+  uint64_t full[NSLOT];        // first CTA's copy counts both CTAs' loads
+  uint64_t empty[NSLOT];       // per CTA, arrived on by the MMA commit
   uint64_t tfull[2];           // per CTA, arrived on by the MMA commit
   uint64_t tempty[2];          // first CTA's copy: every epilogue warp of both CTAs
   uint64_t drain;
@@ -156,7 +155,7 @@ struct SmemCtl {
   uint64_t took;               // first CTA: its producer has started the last published tile
   Tile lsq[SQ];
   Tile xq[SQ];
-  int grow[SQ][MAX_TOK / 2];  // row gather: x row of each of this CTA's token rows of lsq[slot]
+  int grow[SQ][TOK / 2];     // row gather: x row of each of this CTA's token rows of lsq[slot]
   uint32_t tmem_base;
   int abort_flag;
   int nprob;
@@ -167,10 +166,8 @@ struct SmemCtl {
   int row0[MAXP];
 };
 
-template <int GEO>
-constexpr size_t smem_bytes() { return (size_t)Geom<GEO>::STAGES * stage_bytes<GEO>() + sizeof(SmemCtl); }
-static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448,
-              "shared memory budget of one CTA");
+constexpr size_t smem_bytes() { return (size_t)RING_BYTES + sizeof(SmemCtl); }
+static_assert(smem_bytes() <= 232448, "shared memory budget of one CTA");
 
 template <int MODE>
 __device__ __forceinline__ int feat_total(const TcParams& p, bool shared) {
@@ -192,9 +189,8 @@ __device__ __forceinline__ int k_units_of(const TcParams& p, bool shared) {
   return p.H / KU;
 }
 
-template <int MODE, int GEO>
+template <int MODE>
 __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c, int tile) {
-  constexpr int TOK = Geom<GEO>::TOK;
   int lo = 0, hi = c.nprob - 1;  // largest q with tile_start[q] <= tile
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -234,6 +230,27 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   t.kb = (t.ku + UNITS - 1) / UNITS;
   return t;
 }
+
+// Bytes of one unit of this CTA's token rows in a stage of tile t: the boxes it loads, or with
+// the row gather its rows (a multiple of 8 rows: 1 KB aligned, as the 128-byte swizzle wants).
+__device__ __forceinline__ uint32_t tok_unit_bytes(const Tile& t, bool gathered) {
+  if (gathered) return (uint32_t)(t.ncols / 2) * KU * 2;
+  return (uint32_t)t.nbox * (t.big_box ? XBOX_L : XBOX_S) * KU * 2;
+}
+__device__ __forceinline__ uint32_t stage_bytes_of(const Tile& t, bool gathered) {
+  return A_BYTES + UNITS * tok_unit_bytes(t, gathered);
+}
+// Placement of consecutive stages in the ring: each after the previous one, or at the start
+// when it would run past the end. Producer and MMA issuer of both CTAs walk the same sequence of
+// tiles and so place every stage at the same offset.
+struct RingPlace {
+  uint32_t next = 0;
+  __device__ __forceinline__ uint32_t place(uint32_t bytes) {
+    const uint32_t off = next + bytes > RING_BYTES ? 0u : next;
+    next = off + bytes;
+    return off;
+  }
+};
 
 __device__ __forceinline__ Tile end_tile() {
   Tile t;
@@ -448,10 +465,8 @@ __device__ __forceinline__ bool ring_take_warp(SmemCtl& c, uint32_t qs, uint32_t
   return true;
 }
 
-template <int MODE, int GEO>
+template <int MODE, int NS>
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  constexpr int TOK = Geom<GEO>::TOK, STAGES = Geom<GEO>::STAGES;
-  constexpr int B_UNIT = b_unit<GEO>(), STAGE_BYTES = stage_bytes<GEO>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);  // 128-byte swizzle atoms want 1 KB alignment
   uint8_t* sgen = smem_raw;
@@ -459,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     if (threadIdx.x == 0) set_error(p.err, ERR_DEVICE_CHECK);
     return;
   }
-  SmemCtl& c = *reinterpret_cast<SmemCtl*>(sgen + (size_t)STAGES * STAGE_BYTES);
+  SmemCtl& c = *reinterpret_cast<SmemCtl*>(sgen + RING_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();   // 0: issues the MMA; 1: its peer
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
@@ -467,7 +482,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   auto bar = [](const uint64_t& b) { return smem_u32(&b); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(bar(c.full[s]), 1); mbar_init(bar(c.empty[s]), 1); }
+    for (int s = 0; s < NSLOT; ++s) { mbar_init(bar(c.full[s]), 1); mbar_init(bar(c.empty[s]), 1); }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(c.tfull[a]), 1);
       mbar_init(bar(c.tempty[a]), 2 * EPI_WARPS);  // every epilogue warp of both CTAs
@@ -571,10 +586,41 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     }
     const bool hint = p.l2_hints != 0;
     const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
-    uint32_t stage = 0, phase = 0;
-    uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once / its parity
+    uint32_t seq = 0;                           // stages issued so far
+    RingPlace place;
+    uint32_t hlo[NS - 1], hhi[NS - 1];          // ring bytes of stages seq-1, seq-2, ...
+#pragma unroll
+    for (int i = 0; i < NS - 1; ++i) hlo[i] = hhi[i] = 0;
+    uint32_t issued_mask = 0, last_parity = 0;  // per slot: issued at least once / its parity
     uint32_t qs = 0, qph = 0;                   // schedule ring slot and phase
     bool ok = true;
+    // Places stage `seq` (`bytes` long) and names the stage whose release it must wait for:
+    // the latest earlier stage whose bytes it overlaps, or the barrier slot's previous stage
+    // (the MMA commits stages in order, so that one release covers every earlier stage).
+    auto plan = [&](uint32_t bytes, uint32_t& off, uint32_t& slot, int& w) {
+      off = place.place(bytes);
+      w = (int)seq - NS;
+#pragma unroll
+      for (int i = 0; i < NS - 1; ++i) {
+        const int j = (int)seq - 1 - i;
+        if (j > w && off < hhi[i] && hlo[i] < off + bytes) w = j;
+      }
+#pragma unroll
+      for (int i = NS - 2; i > 0; --i) { hlo[i] = hlo[i - 1]; hhi[i] = hhi[i - 1]; }
+      hlo[0] = off;
+      hhi[0] = off + bytes;
+      slot = seq % NS;
+    };
+    auto released = [&](int w) -> bool {
+      if (w < 0) return true;
+      return warp_wait_bounded(bar(c.empty[(uint32_t)w % NS]), ((uint32_t)w / NS) & 1u,
+                               abort_flag, p.err, TIMEOUT_NS);
+    };
+    auto issued = [&](uint32_t slot) {
+      issued_mask |= 1u << slot;
+      last_parity = (last_parity & ~(1u << slot)) | (((seq / NS) & 1u) << slot);
+      ++seq;
+    };
     while (ok) {
       Tile t;
       int4 rows;  // row gather: this lane's four x rows
@@ -589,21 +635,28 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         // routed rows gathered from x: lanes 0 / 1 load the weight box of unit 0 / 1, lane l
         // the x rows 4l .. 4l+3 of this CTA's half of the tile (one gather4 per unit)
         const int half = t.ncols / 2;
-        const uint32_t tok_bytes = (uint32_t)half * KU * 2;
+        const uint32_t tok_bytes = tok_unit_bytes(t, true);
+        const uint32_t sbytes = stage_bytes_of(t, true);
         for (int kb = 0; kb < t.kb; ++kb) {
           const int nu = min(UNITS, t.ku - kb * UNITS);
           const int uw = lane & 1;
           const Boxes b = boxes_of<MODE>(p, t, t.ku0 + kb * UNITS + uw, rank);
           const int kx = (t.ku0 + kb * UNITS) * KU;
-          const uint32_t fb = mapa_shared(bar(c.full[stage]), 0);
-          const uint32_t sa = sbase + stage * STAGE_BYTES + uw * A_UNIT;
-          const uint32_t sg = sbase + stage * STAGE_BYTES + A_BYTES + lane * (4 * KU * 2);
           const uint32_t tx = 2 * nu * (A_UNIT + tok_bytes);
-          if (!warp_wait_bounded(bar(c.empty[stage]), phase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
+          uint32_t off, slot;
+          int w;
+          plan(sbytes, off, slot, w);
+          const uint32_t fb = mapa_shared(bar(c.full[slot]), 0);
+          const uint32_t sa = sbase + off + uw * A_UNIT;
+          const uint32_t sg = sbase + off + A_BYTES + lane * (4 * KU * 2);
+          ready_before(fb); ready_before(sa); ready_before(sg); ready_before(tx);
+          ready_before(b.tw); ready_before((uint32_t)b.ax); ready_before((uint32_t)b.ay0);
+          ready_before((uint32_t)b.ay1); ready_before((uint32_t)kx);
+          if (!released(w)) {
             ok = false;
             break;
           }
-          if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[stage]), tx);
+          if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[slot]), tx);
           __syncwarp();
           if (lane < nu) {
             if (hint) tma_load_5d_pair_hint(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1, pol_w);
@@ -612,15 +665,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
           if (4 * lane < half) {
             tma_gather4_pair(sg, &p.tmXg, fb, kx, rows.x, rows.y, rows.z, rows.w);
             if (nu > 1)
-              tma_gather4_pair(sg + B_UNIT, &p.tmXg, fb, kx + KU, rows.x, rows.y, rows.z, rows.w);
+              tma_gather4_pair(sg + tok_bytes, &p.tmXg, fb, kx + KU, rows.x, rows.y, rows.z,
+                               rows.w);
           }
           __syncwarp();
-          issued_mask |= 1u << stage;
-          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          issued(slot);
         }
         continue;
       }
+      const uint32_t tok_bytes = tok_unit_bytes(t, false);
+      const uint32_t sbytes = stage_bytes_of(t, false);
       for (int kb = 0; kb < t.kb; ++kb) {
         // everything the stage's copies need is computed before waiting for the slot
         const int nu = min(UNITS, t.ku - kb * UNITS);             // units in this block
@@ -629,15 +683,23 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         const int u = (lane >> 3) & 1, j = lane & 7;
         const bool active = lane < 8 * nu;
         const Boxes b = boxes_of<MODE>(p, t, t.ku0 + kb * UNITS + u, rank);
-        const uint32_t fb = mapa_shared(bar(c.full[stage]), 0);  // the first CTA's barrier
-        const uint32_t sa = sbase + stage * STAGE_BYTES + u * A_UNIT;
-        const uint32_t sb = sbase + stage * STAGE_BYTES + A_BYTES + u * B_UNIT + j * b.box_bytes;
-        const uint32_t tx = 2 * nu * (A_UNIT + t.nbox * b.box_bytes);
-        if (!warp_wait_bounded(bar(c.empty[stage]), phase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
+        const uint32_t tx = 2 * nu * (A_UNIT + tok_bytes);
+        uint32_t off, slot;
+        int w;
+        plan(sbytes, off, slot, w);
+        const uint32_t fb = mapa_shared(bar(c.full[slot]), 0);  // the first CTA's barrier
+        const uint32_t sa = sbase + off + u * A_UNIT;
+        const uint32_t sb = sbase + off + A_BYTES + u * tok_bytes + j * b.box_bytes;
+        const int by = b.by0 + j * b.box_rows;
+        ready_before(fb); ready_before(sa); ready_before(sb); ready_before(tx);
+        ready_before(b.tw); ready_before(b.tx); ready_before((uint32_t)b.ax);
+        ready_before((uint32_t)b.ay0); ready_before((uint32_t)b.ay1);
+        ready_before((uint32_t)b.bx); ready_before((uint32_t)by);
+        if (!released(w)) {
           ok = false;
           break;
         }
-        if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[stage]), tx);
+        if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[slot]), tx);
         __syncwarp();
         if (active) {
           if (j == 0) {
@@ -650,26 +712,22 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             }
           }
           if (j < t.nbox) {
-            if (hint) tma_load_2d_pair_hint(sb, b.tx, fb, b.bx, b.by0 + j * b.box_rows, pol_x);
-            else tma_load_2d_pair(sb, b.tx, fb, b.bx, b.by0 + j * b.box_rows);
+            if (hint) tma_load_2d_pair_hint(sb, b.tx, fb, b.bx, by, pol_x);
+            else tma_load_2d_pair(sb, b.tx, fb, b.bx, by);
           }
         }
         __syncwarp();
-        issued_mask |= 1u << stage;
-        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        issued(slot);
       }
     }
-    if (ok) {
-      // tail: wait until the MMA has released every stage (all its commits landed)
-      for (int i = 0; i < STAGES; ++i) {
-        if (!warp_wait_bounded(bar(c.empty[stage]), phase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) break;
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-      }
+    if (ok && seq > 0) {
+      // tail: wait until the MMA has released the last stage (and with it every earlier one)
+      const uint32_t w = seq - 1;
+      warp_wait_bounded(bar(c.empty[w % NS]), (w / NS) & 1u, abort_flag, p.err, TIMEOUT_NS);
     }
     if (*abort_flag && lane == 0) {
       if (rank == 0) {
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < NS; ++s)
           if ((issued_mask >> s) & 1u) grace_wait(bar(c.full[s]), (last_parity >> s) & 1u);
       } else {
         grace_sleep();  // this CTA's loads complete on the other CTA's barriers
@@ -678,7 +736,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   } else if (warp == 1) {
     // ================================================================ MMA issuer (first CTA)
     if (rank == 0 && lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, aphase = 0, qs = 0, qph = 0;
+      uint32_t slot = 0, sphase = 0, acc = 0, aphase = 0, qs = 0, qph = 0;
+      RingPlace place;
       bool ok = true;
       while (ok) {
         Tile t;
@@ -686,6 +745,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         if (++qs == SQ) { qs = 0; qph ^= 1u; }
         if (t.prob < 0) break;
         const uint32_t idesc = idesc_bf16_f32(2 * BM, t.ncols);
+        const bool gathered = MODE == MODE_UP && p.row_token != nullptr && !t.shared;
+        const uint32_t tok_bytes = tok_unit_bytes(t, gathered);
+        const uint32_t sbytes = stage_bytes_of(t, gathered);
         if (!mbar_wait_bounded(bar(c.tempty[acc]), aphase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
           ok = false;
           break;
@@ -693,23 +755,29 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
         for (int kb = 0; kb < t.kb; ++kb) {
-          if (!mbar_wait_bounded(bar(c.full[stage]), phase, abort_flag, p.err, TIMEOUT_NS)) {
+          // the stage's descriptors are ready before its data: nothing but the MMAs follows
+          // the wait
+          const uint32_t sa = sbase + place.place(sbytes);
+          const uint64_t ad0 = sdesc_k_sw128(sa), bd0 = sdesc_k_sw128(sa + A_BYTES);
+          const uint64_t ad1 = ad0 + (A_UNIT >> 4), bd1 = bd0 + (tok_bytes >> 4);
+          const bool two = t.ku - kb * UNITS > 1;
+          const uint32_t acc0 = kb > 0 ? 1u : 0u;
+          ready_before(ad0); ready_before(bd0); ready_before(ad1); ready_before(bd1);
+          if (!mbar_wait_bounded(bar(c.full[slot]), sphase, abort_flag, p.err, TIMEOUT_NS)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const int nu = min(UNITS, t.ku - kb * UNITS);
-          for (int u = 0; u < nu; ++u) {
-            const uint64_t ad = sdesc_k_sw128(sa + u * A_UNIT);
-            const uint64_t bd = sdesc_k_sw128(sa + A_BYTES + u * B_UNIT);
+#pragma unroll
+          for (int kk = 0; kk < KU / 16; ++kk)
+            tc_mma_f16_pair(d_tmem, ad0 + 2u * kk, bd0 + 2u * kk, idesc, kk > 0 ? 1u : acc0);
+          if (two) {
 #pragma unroll
             for (int kk = 0; kk < KU / 16; ++kk)
-              tc_mma_f16_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
-                              (kb > 0 || u > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_f16_pair(d_tmem, ad1 + 2u * kk, bd1 + 2u * kk, idesc, 1u);
           }
-          tc_commit_pair_mc(bar(c.empty[stage]), 0x3);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          tc_commit_pair_mc(bar(c.empty[slot]), 0x3);
+          if (++slot == NS) { slot = 0; sphase ^= 1u; }
         }
         if (!ok) break;
         tc_commit_pair_mc(bar(c.tfull[acc]), 0x3);
@@ -734,7 +802,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       Tile t;
       const TcParams* gp = (MODE == MODE_UP && p.row_token != nullptr) ? &p : nullptr;
       if (rank == 0) {
-        t = cur < total ? decode_tile<MODE, GEO>(p, c, cur) : end_tile();
+        t = cur < total ? decode_tile<MODE>(p, c, cur) : end_tile();
         if (!ring_publish(c, qs, qph, t, abort_flag, p.err, gp, rank) ||
             !ring_send(c, qs, qph, t, abort_flag, p.err))
           break;
@@ -927,7 +995,7 @@ bool make_token_maps(CUtensorMap* big, CUtensorMap* small, const void* base, uin
   return make_map(big, base, inner, outer, XBOX_L) && make_map(small, base, inner, outer, XBOX_S);
 }
 
-template <int MODE, int GEO>
+template <int MODE, int NS>
 cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
   static int grid_for_device[64] = {0};
   int dev = 0;
@@ -943,19 +1011,19 @@ cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes<GEO>();
+  cfg.dynamicSmemBytes = smem_bytes();
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   if (grid == 0) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE, GEO>,
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_bytes<GEO>());
+                                         (int)smem_bytes());
     if (e != cudaSuccess) return e;
     // persistent grid: as many CTA pairs as can be resident at once (one CTA per SM)
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<MODE, GEO>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<MODE, NS>, &cfg);
     if (e != cudaSuccess) return e;
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     grid = 2 * (clusters < num_sms / 2 ? clusters : num_sms / 2);
@@ -963,15 +1031,7 @@ cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
   }
   cfg.gridDim = dim3(grid, 1, 1);
   note_launches(1);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, GEO>, prm);
-}
-
-// Expert GEMMs: the ring geometry follows the batch (a segment never has more rows than T).
-template <int MODE>
-cudaError_t launch_geo(const TcParams& prm, int num_sms, cudaStream_t st) {
-  if (prm.T <= Geom<2>::TOK) return launch_mode<MODE, 2>(prm, num_sms, st);
-  if (prm.T <= Geom<1>::TOK) return launch_mode<MODE, 1>(prm, num_sms, st);
-  return launch_mode<MODE, 0>(prm, num_sms, st);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, NS>, prm);
 }
 
 }  // namespace
@@ -1000,7 +1060,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
     if (!ok) return cudaErrorInvalidValue;
     // Few token tiles (decode): split the K range so that about every CTA pair has a tile;
     // the partial sums go to the caller's scratch and are reduced in a fixed order.
-    const int tiles = (int)((T + Geom<0>::TOK - 1) / Geom<0>::TOK) * (int)((N + 2 * BM - 1) / (2 * BM));
+    const int tiles = (int)((T + TOK - 1) / TOK) * (int)((N + 2 * BM - 1) / (2 * BM));
     const int ku_total = (int)(H / KU);
     const int kb_total = (ku_total + UNITS - 1) / UNITS;
     const int pairs = num_sms / 2;
@@ -1016,7 +1076,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
         prm.gate_part = a.gate_part;
       }
     }
-    cudaError_t e = launch_mode<MODE_GATE, 0>(prm, num_sms, st);
+    cudaError_t e = launch_mode<MODE_GATE, 3>(prm, num_sms, st);
     if (e != cudaSuccess || prm.splits == 1) return e;
     int blocks = (int)(((size_t)T * N + 255) / 256);
     if (blocks > num_sms * 8) blocks = num_sms * 8;
@@ -1037,14 +1097,16 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
     if (a.has_shared) ok = ok && make_up_weight_map(&prm.tmW1, a.b1, H, I, S) &&
                            make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, H, T);
     if (!ok) return cudaErrorInvalidValue;
-    return launch_geo<MODE_UP>(prm, num_sms, st);
+    return prm.T <= kDeepRingMaxTokens ? launch_mode<MODE_UP, NSLOT>(prm, num_sms, st)
+                                       : launch_mode<MODE_UP, 3>(prm, num_sms, st);
   }
   if (a.n_routed > 0) ok = ok && make_map(&prm.tmW0, a.b0, I, N * H, BM) &&
                            make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, I, R);
   if (a.has_shared) ok = ok && make_map(&prm.tmW1, a.b1, I, S * H, BM) &&
                          make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, S * I, T);
   if (!ok) return cudaErrorInvalidValue;
-  return launch_geo<MODE_DOWN>(prm, num_sms, st);
+  return prm.T <= kDeepRingMaxTokens ? launch_mode<MODE_DOWN, NSLOT>(prm, num_sms, st)
+                                     : launch_mode<MODE_DOWN, 3>(prm, num_sms, st);
 }
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long timeout_ns, cudaStream_t st) {
@@ -1052,3 +1114,4 @@ cudaError_t launch_wait_selftest(int* err, unsigned long long timeout_ns, cudaSt
 }
 
 }  // namespace moe
+
