@@ -103,7 +103,8 @@ constexpr int32_t kGatherMaxTokens = 32;
 // Workspace carve for one config and token count. Every region is 256-byte aligned.
 struct Layout {
   size_t u, idx, w, offsets, slot_row, row_token, masks, cnt, base, thr, part_s, part_c, part_lse,
-      counts, recv, seq_s, seq_c, seq_lb, gate_part, sched, xy_perm, h, h_sh, y_sh, total;
+      counts, recv, seq_s, seq_c, seq_lb, gate_part, sched, split_part, xy_perm, h, h_sh, y_sh,
+      total;
 };
 
 Layout layout(const moe_config* c, int32_t T) {
@@ -137,7 +138,8 @@ Layout layout(const moe_config* c, int32_t T) {
   L.seq_c = take(seq_rows * N * 4);
   L.seq_lb = take(Tt * 8);
   L.gate_part = take((size_t)GATE_PART_ROWS * N * 4);
-  L.sched = take(2 * 4);          // tile counters of the up and down GEMMs
+  L.sched = take(kSchedInts * 4);  // tile and split counters of the up and down GEMMs
+  L.split_part = take(c->dtype == MOE_BF16 ? kSplitMaxPieces * kSplitPieceFloats * 4 : 0);
   L.xy_perm = take(A * H * eb);   // x_perm, then reused for y_perm
   L.h = take(A * I * eb);
   L.h_sh = take(Tt * (S > 0 ? S : 1) * I * eb);
@@ -281,18 +283,22 @@ moe_status do_permute(const moe_config* c, int32_t T, const int32_t* idx, const 
   return cuda_status(launch_dispatch(p, num_sms(), st), "row dispatch");
 }
 
-// Zero the up and down GEMMs' tile counters in the workspace (one memset node per FFN).
+// Zero the up and down GEMMs' tile and split counters in the workspace (one memset node per
+// FFN).
 moe_status reset_sched(const moe_config* c, int32_t T, void* ws, cudaStream_t st) {
   if (c->dtype != MOE_BF16) return MOE_OK;
-  return cuda_status(cudaMemsetAsync(at<int32_t>(ws, layout(c, T).sched), 0, 2 * sizeof(int32_t), st),
+  return cuda_status(cudaMemsetAsync(at<int32_t>(ws, layout(c, T).sched), 0,
+                                     kSchedInts * sizeof(int32_t), st),
                      "tile counter reset");
 }
 
-// sched: the two tile counters (up, down) zeroed by reset_sched, or nullptr (static schedule).
+// sched: the workspace's scheduling ints (tile counters of up and down, then their split
+// counters), zeroed by reset_sched or the permutation, or nullptr (static schedule, no tail
+// split). split_part: the workspace's split partial accumulators (used with sched).
 // row_token != nullptr (bf16 only): the routed rows are gathered from x (x_perm unused).
 moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32_t* offsets,
                  const void* x, const moe_weights* w, void* h, void* h_sh, int32_t* sched,
-                 cudaStream_t st, const int32_t* row_token = nullptr) {
+                 float* split_part, cudaStream_t st, const int32_t* row_token = nullptr) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_UP;
@@ -302,6 +308,8 @@ moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32
   g.a0 = row_token != nullptr ? x : x_perm; g.a1 = x; g.b0 = w->w13; g.b1 = w->w13_shared;
   g.out0 = h; g.out1 = h_sh; g.err = error_word();
   g.sched = sched;
+  g.split_cnt = sched ? sched + 2 : nullptr;
+  g.split_part = sched ? split_part : nullptr;
   g.row_token = row_token;
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "expert up GEMM");
@@ -309,7 +317,7 @@ moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32
 
 moe_status do_down(const moe_config* c, int32_t T, const void* h, const int32_t* offsets,
                    const void* h_sh, const moe_weights* w, void* y, void* y_sh, int32_t* sched,
-                   cudaStream_t st) {
+                   float* split_part, cudaStream_t st) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_DOWN;
@@ -319,6 +327,8 @@ moe_status do_down(const moe_config* c, int32_t T, const void* h, const int32_t*
   g.a0 = h; g.a1 = h_sh; g.b0 = w->w2; g.b1 = w->w2_shared;
   g.out0 = y; g.out1 = y_sh; g.err = error_word();
   g.sched = sched ? sched + 1 : nullptr;
+  g.split_cnt = sched ? sched + 2 + kSplitCounters : nullptr;
+  g.split_part = sched ? split_part : nullptr;
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "expert down GEMM");
 }
@@ -391,9 +401,11 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
   TRY(do_permute(cfg, T, idx, wt, x, offsets, row_token, nullptr, slot_row,
                  gather ? nullptr : xy, ws, st, sched));
   stage_mark(STAGE_UP, st);
-  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, sched, st, gather ? row_token : nullptr));
+  float* split_part = at<float>(ws, L.split_part);
+  TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, sched, split_part, st,
+            gather ? row_token : nullptr));
   stage_mark(STAGE_DOWN, st);
-  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, sched, st));  // y_perm overwrites x_perm
+  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, sched, split_part, st));  // y_perm overwrites x_perm
   stage_mark(STAGE_COMBINE, st);
   return do_combine(cfg, T, xy, slot_row, wt, y_sh, out, st);
 }
@@ -522,7 +534,7 @@ moe_status moe_expert_up(const moe_config* cfg, int32_t T, const void* x_perm,
     CHECK_PTR(x);
     CHECK_PTR(h_shared);
   }
-  return do_up(cfg, T, x_perm, offsets, x, w, h, h_shared, nullptr, S_(stream));
+  return do_up(cfg, T, x_perm, offsets, x, w, h, h_shared, nullptr, nullptr, S_(stream));
 }
 
 moe_status moe_expert_up_gather(const moe_config* cfg, int32_t T, const void* x,
@@ -540,7 +552,8 @@ moe_status moe_expert_up_gather(const moe_config* cfg, int32_t T, const void* x,
   CHECK_PTR(offsets);
   CHECK_PTR(h);
   if (cfg->n_shared > 0) CHECK_PTR(h_shared);
-  return do_up(cfg, T, nullptr, offsets, x, w, h, h_shared, nullptr, S_(stream), row_token);
+  return do_up(cfg, T, nullptr, offsets, x, w, h, h_shared, nullptr, nullptr, S_(stream),
+               row_token);
 }
 
 moe_status moe_expert_down(const moe_config* cfg, int32_t T, const void* h,
@@ -557,7 +570,7 @@ moe_status moe_expert_down(const moe_config* cfg, int32_t T, const void* h,
     CHECK_PTR(h_shared);
     CHECK_PTR(y_shared);
   }
-  return do_down(cfg, T, h, offsets, h_shared, w, y_perm, y_shared, nullptr, S_(stream));
+  return do_down(cfg, T, h, offsets, h_shared, w, y_perm, y_shared, nullptr, nullptr, S_(stream));
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const void* x_perm,
@@ -581,8 +594,9 @@ moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const void* x_perm,
   void* h_sh = cfg->n_shared > 0 ? at<char>(ws, L.h_sh) : nullptr;
   int32_t* sched = at<int32_t>(ws, L.sched);
   TRY(reset_sched(cfg, T, ws, S_(stream)));
-  TRY(do_up(cfg, T, x_perm, offsets, x, w, h, h_sh, sched, S_(stream)));
-  return do_down(cfg, T, h, offsets, h_sh, w, y_perm, y_shared, sched, S_(stream));
+  float* split_part = at<float>(ws, L.split_part);
+  TRY(do_up(cfg, T, x_perm, offsets, x, w, h, h_sh, sched, split_part, S_(stream)));
+  return do_down(cfg, T, h, offsets, h_sh, w, y_perm, y_shared, sched, split_part, S_(stream));
 }
 
 moe_status moe_combine(const moe_config* cfg, int32_t T, const void* y_perm,

@@ -119,6 +119,8 @@ struct TcParams {
                              // through L2 once, the activations are read again soon)
   int splits, ku_per_split;  // GATE: K range split over `splits` tiles (1 = no split); units
                              // per split, even
+  float* split_part;         // UP / DOWN tail split (see tail_split): partial accumulators, and
+  int* split_cnt;            // arrival counters (zero at launch); nullptr: no tail split
   int* err;
 };
 
@@ -134,7 +136,8 @@ struct alignas(16) Tile {
   int big_box;   // boxes of 64 rows (else one box of 32)
   int ku0, ku;   // first k unit and k units (GATE split-K: this split's range)
   int kb;        // k blocks (stages): ku / UNITS rounded up
-  int split;     // GATE split-K: which split
+  int split;     // GATE split-K: which split. UP / DOWN: piece | pieces << 8 | split tile << 16
+                 // for a piece of a tail tile (pieces >= 2), else 0
   int shared;    // the shared experts' problem
 };
 constexpr int TILE_WORDS = sizeof(Tile) / 4;
@@ -159,7 +162,9 @@ struct SmemCtl {
   uint32_t tmem_base;
   int abort_flag;
   int nprob;
-  int total_tiles;
+  int total_tiles;            // work items: whole tiles, then the pieces of the split tail tiles
+  int split_first;            // first split tile (== first piece's item)
+  int split_s;                // pieces per split tile (0: no split)
   int tile_start[MAXP + 1];   // by position in `order`
   int order[MAXP];            // problems, most rows first (ties: lower index)
   int rows[MAXP];             // by problem: rows and first row of its segment
@@ -231,6 +236,23 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   return t;
 }
 
+// Work item -> tile: items below split_first are whole tiles; the rest are the pieces of the
+// split tiles, piece fastest, each a contiguous range of the tile's k blocks.
+template <int MODE>
+__device__ __forceinline__ Tile decode_item(const TcParams& p, const SmemCtl& c, int item) {
+  const int S = c.split_s;
+  if (MODE == MODE_GATE || S < 2 || item < c.split_first) return decode_tile<MODE>(p, c, item);
+  const int j = item - c.split_first;
+  const int sid = j / S, piece = j - sid * S;
+  Tile t = decode_tile<MODE>(p, c, c.split_first + sid);
+  const int lo = piece * t.kb / S, hi = (piece + 1) * t.kb / S;
+  t.ku0 = lo * UNITS;
+  t.ku = min(hi * UNITS, t.ku) - t.ku0;
+  t.kb = hi - lo;
+  t.split = piece | (S << 8) | (sid << 16);
+  return t;
+}
+
 // Bytes of one unit of this CTA's token rows in a stage of tile t: the boxes it loads, or with
 // the row gather its rows (a multiple of 8 rows: 1 KB aligned, as the 128-byte swizzle wants).
 __device__ __forceinline__ uint32_t tok_unit_bytes(const Tile& t, bool gathered) {
@@ -251,6 +273,30 @@ struct RingPlace {
     return off;
   }
 };
+
+// Tail split: W whole tiles on P CTA pairs end in a wave of R = W mod P tiles (all W when
+// W < P) that leaves P - R pairs idle. When R <= P / 2, each of those R tiles is cut along K
+// into S = P / R pieces (at most 8, and at least kSplitMinBlocks k blocks of a routed tile
+// each: a piece pays its own ring fill and partial round trip), which run as the last work
+// items. Sets first = W - R and pieces = S, or pieces = 0 (no split). Only the up projection
+// splits: its tiles run over the hidden size (56 k blocks at 7168); the down projection's run
+// over one expert's intermediate size, and measured at 2048 (16 k blocks, two pieces) the
+// pieces' ring fills cost more than the shorter wave saves.
+constexpr int kSplitMinBlocks = 8;
+__device__ __forceinline__ void tail_split(int W, int P, int kb_routed, int& first, int& pieces) {
+  first = W;
+  pieces = 0;
+  if (W <= 0 || P <= 1) return;
+  const int R = W % P;
+  if (R == 0 || 2 * R > P || R > kSplitMaxTiles) return;
+  int S = P / R;
+  S = min(S, 8);
+  S = min(S, kb_routed / kSplitMinBlocks);
+  S = min(S, kSplitMaxPieces / R);
+  if (S < 2) return;
+  first = W - R;
+  pieces = S;
+}
 
 __device__ __forceinline__ Tile end_tile() {
   Tile t;
@@ -556,7 +602,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       if (i < nprob) c.tile_start[i] = run + incl - cnt;
       run += __shfl_sync(FULL_MASK, incl, 31);
     }
-    if (lane == 0) { c.tile_start[nprob] = run; c.total_tiles = run; c.nprob = nprob; }
+    if (lane == 0) {
+      c.tile_start[nprob] = run;
+      c.nprob = nprob;
+      int first = run, pieces = 0;
+      if (MODE == MODE_UP && p.split_part != nullptr && p.split_cnt != nullptr)
+        tail_split(run, (int)(gridDim.x >> 1), (k_units_of<MODE>(p, false) + UNITS - 1) / UNITS,
+                   first, pieces);
+      c.split_first = first;
+      c.split_s = pieces;
+      c.total_tiles = first + (run - first) * (pieces > 1 ? pieces : 1);
+    }
   }
   // both CTAs' barriers are initialised before either CTA signals the other's
   tc_fence_before();
@@ -802,7 +858,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       Tile t;
       const TcParams* gp = (MODE == MODE_UP && p.row_token != nullptr) ? &p : nullptr;
       if (rank == 0) {
-        t = cur < total ? decode_tile<MODE>(p, c, cur) : end_tile();
+        t = cur < total ? decode_item<MODE>(p, c, cur) : end_tile();
         if (!ring_publish(c, qs, qph, t, abort_flag, p.err, gp, rank) ||
             !ring_send(c, qs, qph, t, abort_flag, p.err))
           break;
@@ -839,23 +895,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
       const int fc = t.f0 + (int)rank * feat_per_cta<MODE>();  // this CTA's first feature
       const int nch = (t.nrows + 31) / 32;
-      if (h >= nch) {
-        // no chunk of this tile for this warp: the accumulator is free as far as it goes
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
-      }
-      for (int ch = h; ch < nch; ch += 2) {
+      // Epilogue of chunk ch (32 tokens) from accumulator values v (fp32 bit patterns).
+      auto emit = [&](const uint32_t (&v)[32], int ch) {
         const int nvalid = t.nrows - ch * 32;
         const size_t row0 = (size_t)(t.r0 + ch * 32);
-        uint32_t v[32];
-        tmem_ld_32cols(tb + ch * 32, v);
-        tmem_wait_ld_fence(v);
-        if (ch + 2 >= nch) {
-          // this warp's share of the accumulator read: hand it back before the stores
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
-        }
         if (MODE == MODE_UP) {
           // lanes 0..15: gate of features fq + lane; lanes 16..31: up of features fq + lane - 16.
           // Lane l < 16 computes tokens 0..15 with its partner's up values, lane l + 16 tokens
@@ -892,6 +935,71 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (fvalid && i < nvalid) out[(size_t)i * p.N] = __uint_as_float(v[i]) + bias;
+          }
+        }
+      };
+      const int pieces = MODE == MODE_GATE ? 0 : (t.split >> 8) & 0xff;
+      if (h >= nch) {
+        // no chunk of this tile for this warp: the accumulator is free as far as it goes
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
+      } else if (pieces < 2) {
+        for (int ch = h; ch < nch; ch += 2) {
+          uint32_t v[32];
+          tmem_ld_32cols(tb + ch * 32, v);
+          tmem_wait_ld_fence(v);
+          if (ch + 2 >= nch) {
+            // this warp's share of the accumulator read: hand it back before the stores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
+          }
+          emit(v, ch);
+        }
+      } else {
+        // a piece of a split tile: park this warp's share of the partial accumulator (fp32, in
+        // L2), count it in; the warp that completes the count adds the pieces in piece order and
+        // runs the epilogue for its share, then sets the counter back to zero
+        const int piece = t.split & 0xff, sid = t.split >> 16;
+        const size_t share = ((size_t)rank * 4 + q) * (TOK * 32);
+        float* mine = p.split_part + (size_t)(sid * pieces + piece) * kSplitPieceFloats + share;
+        for (int ch = h; ch < nch; ch += 2) {
+          uint32_t v[32];
+          tmem_ld_32cols(tb + ch * 32, v);
+          tmem_wait_ld_fence(v);
+          if (ch + 2 >= nch) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (ch * 32 + i < t.nrows) __stcg(mine + (ch * 32 + i) * 32 + lane, __uint_as_float(v[i]));
+        }
+        __threadfence();
+        __syncwarp();
+        int* cnt = p.split_cnt + sid * kSplitWarps + (int)rank * EPI_WARPS + (warp - 2);
+        int before = 0;
+        if (lane == 0) before = atomicAdd(cnt, 1);
+        before = __shfl_sync(FULL_MASK, before, 0);
+        if (before == pieces - 1) {
+          __threadfence();
+          if (lane == 0) atomicExch(cnt, 0);
+          const float* all = p.split_part + (size_t)sid * pieces * kSplitPieceFloats + share;
+          for (int ch = h; ch < nch; ch += 2) {
+            float a[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = 0.0f;
+            for (int s = 0; s < pieces; ++s) {
+              const float* ps = all + (size_t)s * kSplitPieceFloats + (ch * 32) * 32 + lane;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (ch * 32 + i < t.nrows) a[i] += __ldcg(ps + i * 32);
+            }
+            uint32_t v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(a[i]);
+            emit(v, ch);
           }
         }
       }
@@ -1053,6 +1161,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   // small batches: every weight tile is read by one CTA pair, while the token rows and outputs are
   // read again by the next stage (x_perm / h / y_perm fit in L2)
   prm.l2_hints = (a.mode != MODE_GATE && a.T <= kL2HintMaxTokens) ? 1 : 0;
+  if (a.mode != MODE_GATE && a.sched != nullptr) {
+    prm.split_part = a.split_part;
+    prm.split_cnt = a.split_cnt;
+  }
   const uint64_t H = a.H, I = a.I, S = a.S, N = a.N, T = a.T, R = a.rows_cap;
   bool ok = true;
   if (a.mode == MODE_GATE) {

@@ -108,7 +108,7 @@ struct PermuteArgs {
   int32_t* cnt;         // [nb, N]
   int32_t* base;        // [nb, N]
   unsigned long long* thr;  // [D]
-  int32_t* sched_zero;  // nullptr, or two tile counters the permutation sets to zero (the expert
+  int32_t* sched_zero;  // nullptr, or kSchedInts scheduling ints the permutation zeroes (the expert
                         // GEMMs that follow claim tiles from them)
   int* err;
 };
@@ -155,8 +155,23 @@ struct GemmArgs {
                             // tile schedule; nullptr: static round-robin schedule
   const int32_t* row_token; // UP (tcgen05) row gather: routed row r is x[row_token[r]], with
                             // a0 = x [T,H]; nullptr: a0 = x_perm
+  float* split_part;        // UP / DOWN (tcgen05): fp32 partial accumulators of the tail tiles
+                            // split along K (kSplitMaxPieces pieces), or nullptr (no split)
+  int* split_cnt;           // UP / DOWN: kSplitCounters arrival counters of those pieces, zero
+                            // at launch (the last arrival sets its counter back to zero)
   int* err;
 };
+// Tail split of the expert GEMMs: tiles of the last, partly filled wave are cut along K into
+// pieces that idle CTA pairs take; the last piece of a tile to finish adds the pieces' fp32
+// partial accumulators in piece order and runs the epilogue.
+constexpr int kSplitMaxTiles = 40;                    // split tiles per launch at most
+constexpr int kSplitWarps = 16;                       // epilogue warps of a CTA pair
+constexpr int kSplitCounters = kSplitMaxTiles * kSplitWarps;
+constexpr int kSplitMaxPieces = 80;                   // pieces per launch at most
+constexpr size_t kSplitPieceFloats = 2 * 128 * 256;   // a pair's 256 x 256 fp32 accumulator
+// Ints of the workspace's scheduling region: the up and down GEMMs' tile counters, then the
+// up and down GEMMs' split counters. The permutation (or a memset) zeroes all of it.
+constexpr int kSchedInts = 2 + 2 * kSplitCounters;
 // Rows (of N floats) of the gate GEMM's split-K scratch the workspace provides.
 constexpr int GATE_PART_ROWS = 16384;
 // bf16 on tcgen05 / TMEM / TMA (gemm_tc.cu)

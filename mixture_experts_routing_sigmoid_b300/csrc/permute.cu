@@ -195,10 +195,9 @@ __global__ void __launch_bounds__(256) perm_scan_kernel(PermuteArgs p, int nb) {
     p.offsets[e] = off;
     for (int b = 0; b < nb; ++b) p.base[(size_t)b * p.N + e] += off;
   }
-  if (e == 0) {
-    p.offsets[p.N] = excl[p.N];
-    if (p.sched_zero != nullptr) { p.sched_zero[0] = 0; p.sched_zero[1] = 0; }
-  }
+  if (e == 0) p.offsets[p.N] = excl[p.N];
+  if (blockIdx.x == 0 && p.sched_zero != nullptr)
+    for (int i = e; i < kSchedInts; i += blockDim.x) p.sched_zero[i] = 0;
 }
 
 __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
@@ -277,9 +276,10 @@ __global__ void __launch_bounds__(SB_MAX_T) perm_small_kernel(PermuteArgs p) {
     if (blockIdx.x == 0) {
       if (e < p.N) p.offsets[e] = before + incl - c;
       if (e == p.N - 1) p.offsets[p.N] = before + incl;
-      if (e == 0 && p.sched_zero != nullptr) { p.sched_zero[0] = 0; p.sched_zero[1] = 0; }
     }
   }
+  if (blockIdx.x == 0 && p.sched_zero != nullptr)
+    for (int i = threadIdx.x; i < kSchedInts; i += blockDim.x) p.sched_zero[i] = 0;
   __syncthreads();
   if (t < p.T) {
     const int wi = t >> 5;

@@ -84,3 +84,54 @@ def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
     s = np.sort(rng.choice(T, size=n, replace=False))
     # always include the first and last token (tile edges)
     return np.unique(np.concatenate([[0, T - 1], s]))
+
+
+
+def gemm_tiles(cfg: LayerConfig, offs, mode: str):
+    """The expert GEMM's tiles in the kernel's order, restated from its tile rule: problems by
+    decreasing rows (ties: lower index; the shared experts are problem n_routed with T rows),
+    then feature tiles (up: 128 intermediate features, down: 256 hidden features), then token
+    tiles (a segment's rows cut into equal tiles of at most 256, multiples of 16).
+    Returns [(problem, first feature, end feature, first row, end row)], rows relative to the
+    problem's segment."""
+    rows = [int(r) for r in np.diff(np.asarray(offs))]
+    if cfg.n_shared > 0:
+        rows.append(cfg.T)
+    order = sorted(range(len(rows)), key=lambda q: (-rows[q], q))
+    out = []
+    for q in order:
+        r = rows[q]
+        if r <= 0:
+            continue
+        shared = q == cfg.n_routed
+        if mode == "up":
+            feats, per_tile = (cfg.n_shared * cfg.inter if shared else cfg.inter), 128
+        else:
+            feats, per_tile = cfg.hidden, 256
+        ntt = -(-r // 256)
+        per = (-(-r // ntt) + 15) // 16 * 16
+        for ft in range(-(-feats // per_tile)):
+            for tt in range(ntt):
+                out.append((q, ft * per_tile, min(feats, (ft + 1) * per_tile), tt * per,
+                            min(r, (tt + 1) * per)))
+    return out
+
+
+def gemm_tail_split(cfg: LayerConfig, offs, mode: str, pairs: int = 74):
+    """The up projection's tail split (the down projection cuts nothing), restated from the
+    kernel's rule to tell the tests which tiles it cuts along K: with W tiles (gemm_tiles) on
+    `pairs` CTA pairs, the last R = W mod pairs tiles (all W when W < pairs) are cut into
+    S = min(pairs // R, 8, routed k blocks // 8, 80 // R) pieces when R <= pairs / 2, R <= 40
+    and S >= 2. Returns (W, R, S), with R = S = 0 when nothing is split."""
+    W = len(gemm_tiles(cfg, offs, mode))
+    if mode != "up":
+        return W, 0, 0
+    k_routed = cfg.hidden if mode == "up" else cfg.inter
+    kb = -(-(k_routed // 64) // 2)
+    if W <= 0 or pairs <= 1:
+        return W, 0, 0
+    R = W % pairs
+    if R == 0 or 2 * R > pairs or R > 40:
+        return W, 0, 0
+    S = min(pairs // R, 8, kb // 8, 80 // R)
+    return (W, R, S) if S >= 2 else (W, 0, 0)

@@ -10,13 +10,14 @@ import torch
 
 import oracle
 from moe_inputs import CONFIGS, make_logits, make_router, make_weights, make_x
-from tests.helpers import MID_A, MID_B, MID_ODD, MID_V2, rel_frob, sample_tokens, tol_for, workspace
+from tests.helpers import (MID_A, MID_B, MID_ODD, MID_V2, gemm_tail_split, gemm_tiles, rel_frob,
+                           sample_tokens, tol_for, workspace)
 
 pytestmark = pytest.mark.gpu
 
 CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_odd": MID_ODD,
-        # batches of at most 64 and 128 tokens run the expert GEMMs with the 64- and 128-token
-        # ring geometries (more stages of fewer token rows)
+        # batches of at most 64 and 128 tokens: tiles of few token rows, whose smaller ring
+        # stages run deeper
         "mid_a_t50": MID_A.replace(name="mid_a_t50", T=50),
         "mid_odd_t100": MID_ODD.replace(name="mid_odd_t100", T=100)}
 
@@ -125,11 +126,15 @@ def test_combine(name):
         assert np.all(np.abs(got - want) <= 2 ** -8 * np.abs(want) + 1e-2)
 
 
-@pytest.mark.parametrize("name", ["mid_a", "mid_a_t50", "mid_odd_t100", "v3_prefill_e32"])
+@pytest.mark.parametrize("name", ["mid_a", "mid_a_t50", "mid_odd_t100", "v3_prefill_e32",
+                                  "v3_decode_32"])
 def test_tile_schedule_does_not_change_results(name):
-    """moe_expert_ffn (workspace given: tiles claimed dynamically from a counter) and
-    moe_expert_up + moe_expert_down (no workspace: static round-robin tiles) compute every output
-    tile with the same k order, so their outputs are bitwise equal."""
+    """moe_expert_ffn (workspace given: tiles claimed dynamically from a counter, the tail wave's
+    tiles cut along K into pieces) and moe_expert_up + moe_expert_down (no workspace: static
+    round-robin tiles, nothing cut) compute every uncut tile with the same k order, so those
+    outputs are bitwise equal. A cut tile's pieces are added in piece order in fp32: its outputs
+    (and, for a cut up-projection tile, the rows of y it feeds) agree within a bf16 rounding,
+    and two runs are bitwise equal whichever piece finishes last."""
     import mixture_experts_routing_sigmoid_b300 as moe
     cfg = CFGS[name]
     T, H, K, I, S = cfg.T, cfg.hidden, cfg.top_k, cfg.inter, cfg.n_shared
@@ -141,19 +146,48 @@ def test_tile_schedule_does_not_change_results(name):
     x_perm = torch.zeros((T * K, H), dtype=x.dtype, device=dev)
     x_perm[:R] = x[torch.from_numpy(row_token).long().to(dev)]
     offs_d = torch.from_numpy(offs).to(dev)
-    y_dyn = torch.zeros((T * K, H), dtype=x.dtype, device=dev)
-    ys_dyn = torch.zeros((T, H), dtype=x.dtype, device=dev)
-    moe.moe_expert_ffn(cfg, T, x_perm, offs_d, x, w, y_dyn, ys_dyn, workspace(cfg, T))
+    runs = []
+    for _ in range(2):
+        y_dyn = torch.zeros((T * K, H), dtype=x.dtype, device=dev)
+        ys_dyn = torch.zeros((T, H), dtype=x.dtype, device=dev)
+        moe.moe_expert_ffn(cfg, T, x_perm, offs_d, x, w, y_dyn, ys_dyn, workspace(cfg, T))
+        runs.append((y_dyn, ys_dyn))
     h = torch.zeros((T * K, I), dtype=x.dtype, device=dev)
     h_sh = torch.zeros((T, S * I), dtype=x.dtype, device=dev)
-    y_st = torch.zeros_like(y_dyn)
-    ys_st = torch.zeros_like(ys_dyn)
+    y_st = torch.zeros_like(runs[0][0])
+    ys_st = torch.zeros_like(runs[0][1])
     moe.moe_expert_up(cfg, T, x_perm, offs_d, x, w, h, h_sh)
     moe.moe_expert_down(cfg, T, h, offs_d, h_sh, w, y_st, ys_st)
     torch.cuda.synchronize()
     assert moe.moe_get_error() == 0
-    assert torch.equal(y_dyn[:R], y_st[:R])
-    assert torch.equal(ys_dyn, ys_st)
+    (y_dyn, ys_dyn), (y_dyn2, ys_dyn2) = runs
+    assert torch.equal(y_dyn[:R], y_dyn2[:R]) and torch.equal(ys_dyn, ys_dyn2)
+    # outputs that a cut tile computes or feeds
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    cut_y = np.zeros((R, H), bool)
+    cut_ys = np.zeros((T, H), bool)
+    n_cut = 0
+    for mode in ("up", "down"):
+        _, n_tail, pieces = gemm_tail_split(cfg, offs, mode, pairs)
+        if pieces < 2:
+            continue
+        n_cut += n_tail
+        for q, f0, f1, r0, r1 in gemm_tiles(cfg, offs, mode)[-n_tail:]:
+            cols = slice(None) if mode == "up" else slice(f0, f1)
+            if q == cfg.n_routed:
+                cut_ys[r0:r1, cols] = True
+            else:
+                cut_y[offs[q] + r0:offs[q] + r1, cols] = True
+    if name in ("v3_prefill_e32", "v3_decode_32"):
+        assert n_cut > 0, "this batch must exercise the tail split"
+    for got, want, cut in ((y_dyn[:R], y_st[:R], cut_y), (ys_dyn, ys_st, cut_ys)):
+        g = got.float().cpu().numpy()
+        e = want.float().cpu().numpy()
+        np.testing.assert_array_equal(g[~cut], e[~cut])
+        if cut.any():
+            assert np.all(np.abs(g[cut] - e[cut]) <= 2 ** -6 * np.abs(e[cut])
+                          + 1e-3 * np.abs(e).max())
+            assert rel_frob(g[cut], e[cut]) <= 1e-3
 
 
 @pytest.mark.parametrize("name", ["mid_a", "mid_odd", "mid_v2", "mid_a_t50", "mid_odd_t100",
