@@ -99,6 +99,7 @@ constexpr int TOK = 256;                 // tokens per tile at most (MMA N)
 constexpr uint32_t RING_BYTES = 200 * 1024;
 constexpr int NSLOT = 6;                 // more than the stages that fit at once
 constexpr int kDeepRingMaxTokens = 512;
+constexpr int kGateMaxSplits = 16;
 
 struct TcParams {
   CUtensorMap tmW0, tmW1;    // weights: routed, shared (box 128 rows; UP: interleaved 5-D box)
@@ -1170,14 +1171,16 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   if (a.mode == MODE_GATE) {
     ok = make_map(&prm.tmW0, a.b0, H, N, BM) && make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, T);
     if (!ok) return cudaErrorInvalidValue;
-    // Few token tiles (decode): split the K range so that about every CTA pair has a tile;
-    // the partial sums go to the caller's scratch and are reduced in a fixed order.
+    // Few token tiles (decode): split the K range over up to kGateMaxSplits pairs per tile; the
+    // partial sums go to the caller's scratch and are reduced in a fixed order. (Measured at
+    // 32-512 tokens: more, shorter splits only add partial traffic; 16 is 1-3 us faster than
+    // one split per pair.)
     const int tiles = (int)((T + TOK - 1) / TOK) * (int)((N + 2 * BM - 1) / (2 * BM));
     const int ku_total = (int)(H / KU);
     const int kb_total = (ku_total + UNITS - 1) / UNITS;
     const int pairs = num_sms / 2;
     if (a.gate_part != nullptr && 2 * tiles <= pairs) {
-      int want = pairs / tiles;
+      int want = min(pairs / tiles, kGateMaxSplits);
       const size_t fit = a.gate_part_floats / ((size_t)T * N);
       if ((size_t)want > fit) want = (int)fit;
       if (want > kb_total) want = kb_total;
