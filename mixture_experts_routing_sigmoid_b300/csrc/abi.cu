@@ -296,9 +296,12 @@ moe_status reset_sched(const moe_config* c, int32_t T, void* ws, cudaStream_t st
 // counters), zeroed by reset_sched or the permutation, or nullptr (static schedule, no tail
 // split). split_part: the workspace's split partial accumulators (used with sched).
 // row_token != nullptr (bf16 only): the routed rows are gathered from x (x_perm unused).
+// offsets_early: the offsets were written at least two kernels back in the stream (or before a
+// memset node), so the GEMM builds its tile schedule before waiting for the kernel just ahead.
 moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32_t* offsets,
                  const void* x, const moe_weights* w, void* h, void* h_sh, int32_t* sched,
-                 float* split_part, cudaStream_t st, const int32_t* row_token = nullptr) {
+                 float* split_part, cudaStream_t st, const int32_t* row_token = nullptr,
+                 bool offsets_early = false) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_UP;
@@ -311,13 +314,14 @@ moe_status do_up(const moe_config* c, int32_t T, const void* x_perm, const int32
   g.split_cnt = sched ? sched + 2 : nullptr;
   g.split_part = sched ? split_part : nullptr;
   g.row_token = row_token;
+  g.offsets_early = offsets_early ? 1 : 0;
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "expert up GEMM");
 }
 
 moe_status do_down(const moe_config* c, int32_t T, const void* h, const int32_t* offsets,
                    const void* h_sh, const moe_weights* w, void* y, void* y_sh, int32_t* sched,
-                   float* split_part, cudaStream_t st) {
+                   float* split_part, cudaStream_t st, bool offsets_early = false) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   g.mode = MODE_DOWN;
@@ -329,6 +333,7 @@ moe_status do_down(const moe_config* c, int32_t T, const void* h, const int32_t*
   g.sched = sched ? sched + 1 : nullptr;
   g.split_cnt = sched ? sched + 2 + kSplitCounters : nullptr;
   g.split_part = sched ? split_part : nullptr;
+  g.offsets_early = offsets_early ? 1 : 0;
   cudaError_t e = c->dtype == MOE_BF16 ? launch_gemm_tc(g, num_sms(), st) : launch_gemm_simt(g, st);
   return cuda_status(e, "expert down GEMM");
 }
@@ -402,10 +407,13 @@ moe_status layer_steps(const moe_config* cfg, int32_t T, const void* x, const mo
                  gather ? nullptr : xy, ws, st, sched));
   stage_mark(STAGE_UP, st);
   float* split_part = at<float>(ws, L.split_part);
+  // the up GEMM follows the permutation directly when it gathers, else the dispatch; the down
+  // GEMM follows the up GEMM
   TRY(do_up(cfg, T, xy, offsets, x, w, h, h_sh, sched, split_part, st,
-            gather ? row_token : nullptr));
+            gather ? row_token : nullptr, /*offsets_early=*/!gather));
   stage_mark(STAGE_DOWN, st);
-  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, sched, split_part, st));  // y_perm overwrites x_perm
+  TRY(do_down(cfg, T, h, offsets, h_sh, w, xy, y_sh, sched, split_part, st,
+              /*offsets_early=*/true));  // y_perm overwrites x_perm
   stage_mark(STAGE_COMBINE, st);
   return do_combine(cfg, T, xy, slot_row, wt, y_sh, out, st);
 }
@@ -595,8 +603,11 @@ moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const void* x_perm,
   int32_t* sched = at<int32_t>(ws, L.sched);
   TRY(reset_sched(cfg, T, ws, S_(stream)));
   float* split_part = at<float>(ws, L.split_part);
-  TRY(do_up(cfg, T, x_perm, offsets, x, w, h, h_sh, sched, split_part, S_(stream)));
-  return do_down(cfg, T, h, offsets, h_sh, w, y_perm, y_shared, sched, split_part, S_(stream));
+  // after the memset node: the caller's offsets are complete before either GEMM starts
+  TRY(do_up(cfg, T, x_perm, offsets, x, w, h, h_sh, sched, split_part, S_(stream), nullptr,
+            /*offsets_early=*/true));
+  return do_down(cfg, T, h, offsets, h_sh, w, y_perm, y_shared, sched, split_part, S_(stream),
+                 /*offsets_early=*/true);
 }
 
 moe_status moe_combine(const moe_config* cfg, int32_t T, const void* y_perm,

@@ -34,6 +34,7 @@
 // equal token tiles). The first wave is one tile per CTA pair; after that a pair claims the next
 // index from a counter when its producer starts the current tile (round robin without a
 // counter), so the pairs sharing a weight tile run it together and its second read hits L2.
+// (Claiming later, a few k blocks before the current tile's end, measured 1.5-3% slower.)
 //   warp 0      TMA producer (both CTAs): this CTA's weight rows and token rows of one k block
 //               per stage, in a 200 KB ring of stages sized by the tile (below). A k block is
 //               128 elements, two 128-byte-swizzled units of 64 (one TMA box per operand and
@@ -69,6 +70,7 @@ constexpr int BM = 128;                  // weight rows per CTA and operand (MMA
 constexpr int KU = 64;                   // reduction elements per unit (128 bytes of bf16)
 constexpr int UNITS = 2;                 // units per stage (k block of 128 elements)
 constexpr int MAXP = 258;
+constexpr int MAXP4 = (MAXP + 3) & ~3;
 constexpr int THREADS = 352;
 constexpr int EPI_WARPS = 8;             // warps 2 .. 9
 constexpr int SCHED_WARP = 10;
@@ -122,6 +124,9 @@ struct TcParams {
                              // per split, even
   float* split_part;         // UP / DOWN tail split (see tail_split): partial accumulators, and
   int* split_cnt;            // arrival counters (zero at launch); nullptr: no tail split
+  int offsets_early;         // 1: the offsets come from a kernel at least two launches back (the
+                             // kernel ahead waited for it before letting this one start), so the
+                             // tile schedule is built before waiting for the kernel ahead
   int* err;
 };
 
@@ -168,6 +173,8 @@ struct SmemCtl {
   int split_s;                // pieces per split tile (0: no split)
   int tile_start[MAXP + 1];   // by position in `order`
   int order[MAXP];            // problems, most rows first (ties: lower index)
+  alignas(16) uint32_t key[MAXP4];  // sort keys: rows high, reversed index low (0 past nprob)
+  int chunk[THREADS / 32];    // per warp: its 32 positions' tile total
   int rows[MAXP];             // by problem: rows and first row of its segment
   int row0[MAXP];
 };
@@ -235,6 +242,27 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   }
   t.kb = (t.ku + UNITS - 1) / UNITS;
   return t;
+}
+
+// Checked build: a tile whose rows, features, k range or split fields leave their tensors (a
+// corrupt schedule) is reported and its stores are skipped.
+template <int MODE>
+__device__ __forceinline__ bool tile_in_range(const TcParams& p, const Tile& t) {
+  const int nprob = (MODE == MODE_GATE) ? 1 : p.n_routed + p.has_shared;
+  const int rows = (MODE == MODE_GATE || t.shared) ? p.T : p.rows_cap;
+  bool ok = t.prob >= 0 && t.prob < nprob && t.r0 >= 0 && t.nrows >= 1 && t.nrows <= TOK &&
+            t.ncols >= t.nrows && t.ncols <= TOK && t.r0 + t.nrows <= rows && t.f0 >= 0 &&
+            t.f0 < feat_total<MODE>(p, t.shared) && t.kb >= 1 && t.ku0 >= 0 &&
+            t.ku0 + t.ku <= k_units_of<MODE>(p, t.shared);
+  if (MODE == MODE_GATE) {
+    ok = ok && t.split >= 0 && t.split < p.splits;
+  } else {
+    const int pieces = (t.split >> 8) & 0xff, piece = t.split & 0xff, sid = t.split >> 16;
+    ok = ok && (pieces < 2 ? t.split == 0
+                           : (piece < pieces && sid < kSplitMaxTiles &&
+                              (sid + 1) * pieces <= kSplitMaxPieces));
+  }
+  return ok;
 }
 
 // Work item -> tile: items below split_first are whole tiles; the rest are the pieces of the
@@ -550,18 +578,26 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(&c.tmem_base), TMEM_COLS);
 
-  // the kernel ahead in the stream (permutation, or the up projection for the down one) has
-  // finished and its writes are visible from here on
-  pdl_wait();
-  pdl_trigger();
+  // The kernel ahead in the stream has finished and its writes are visible after pdl_wait.
+  // The schedule below reads only the segment offsets; when they come from further back
+  // (offsets_early) it is built first, overlapping the end of the kernel ahead.
+  const bool early = MODE != MODE_GATE && p.offsets_early != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   // ---- problems in order of decreasing rows, so that the longest run first and the pairs
   // finish together; then the tile prefix over that order (counts depend on device offsets)
   const int nprob = (MODE == MODE_GATE) ? 1 : p.n_routed + p.has_shared;
-  for (int q = threadIdx.x; q < nprob; q += THREADS) {
+  for (int q = threadIdx.x; q < MAXP4; q += THREADS) {
+    if (q >= nprob) {
+      c.key[q] = 0u;  // below every problem's key
+      continue;
+    }
     int rows = p.T, row0 = 0;
     if (MODE != MODE_GATE && q < p.n_routed) {
-      row0 = p.offsets[q];
-      const int end = p.offsets[q + 1];
+      row0 = __ldcg(p.offsets + q);
+      const int end = __ldcg(p.offsets + q + 1);
       rows = max(end - row0, 0);
       if (kChecks && (row0 < 0 || end < row0 || end > p.rows_cap)) {
         set_error(p.err, ERR_DEVICE_CHECK);  // a segment outside the rows: skip the problem
@@ -571,39 +607,47 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     }
     c.rows[q] = rows;
     c.row0[q] = row0;
+    // distinct keys (the reversed index in the low bits): the ranks are a permutation
+    c.key[q] = (uint32_t)min(rows, (1 << 22) - 1) << 9 | (uint32_t)(511 - q);
   }
   __syncthreads();
   for (int q = threadIdx.x; q < nprob; q += THREADS) {
-    const int rq = c.rows[q];
+    const uint32_t kq = c.key[q];
     int rank = 0;
-    for (int o = 0; o < nprob; ++o) {
-      const int ro = c.rows[o];
-      rank += (ro > rq || (ro == rq && o < q)) ? 1 : 0;
+    for (int o = 0; o < nprob; o += 4) {  // four keys per shared load
+      const uint4 k4 = *reinterpret_cast<const uint4*>(&c.key[o]);
+      rank += (k4.x > kq) + (k4.y > kq) + (k4.z > kq) + (k4.w > kq);
     }
     c.order[rank] = q;
   }
   __syncthreads();
-  if (warp == 0) {
-    int run = 0;
-    for (int b = 0; b < nprob; b += 32) {
-      const int i = b + lane;       // position in the order
-      int cnt = 0;
-      if (i < nprob) {
-        const int q = c.order[i];
-        const bool sh = (MODE != MODE_GATE) && q >= p.n_routed;
-        cnt = ((c.rows[q] + TOK - 1) / TOK) * n_feat_tiles<MODE>(p, sh);
-        if (MODE == MODE_GATE) cnt *= p.splits;
-      }
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(FULL_MASK, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (i < nprob) c.tile_start[i] = run + incl - cnt;
-      run += __shfl_sync(FULL_MASK, incl, 31);
+  // tile prefix over the order: thread i counts position i's tiles; warp scans, then the warp
+  // totals (nprob <= MAXP < THREADS, so one pass)
+  int cnt = 0, incl = 0;
+  {
+    const int i = threadIdx.x;
+    if (i < nprob) {
+      const int q = c.order[i];
+      const bool sh = (MODE != MODE_GATE) && q >= p.n_routed;
+      cnt = ((c.rows[q] + TOK - 1) / TOK) * n_feat_tiles<MODE>(p, sh);
+      if (MODE == MODE_GATE) cnt *= p.splits;
     }
-    if (lane == 0) {
+    incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) c.chunk[warp] = incl;
+  }
+  __syncthreads();
+  {
+    const int i = threadIdx.x;
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += c.chunk[w];
+    if (i < nprob) c.tile_start[i] = before + incl - cnt;
+    if (i == THREADS - 1) {  // the last thread: every warp's total is before it or its own
+      const int run = before + incl;
       c.tile_start[nprob] = run;
       c.nprob = nprob;
       int first = run, pieces = 0;
@@ -620,6 +664,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   __syncthreads();
   cluster_sync();
   tc_fence_after();
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const uint32_t tmem_base = c.tmem_base;
   const int total = c.total_tiles;
   volatile int* abort_flag = &c.abort_flag;
@@ -895,9 +943,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
       const int fc = t.f0 + (int)rank * feat_per_cta<MODE>();  // this CTA's first feature
+      const bool stores = !kChecks || tile_in_range<MODE>(p, t);
+      if (!stores && lane == 0) set_error(p.err, ERR_DEVICE_CHECK);
       const int nch = (t.nrows + 31) / 32;
       // Epilogue of chunk ch (32 tokens) from accumulator values v (fp32 bit patterns).
       auto emit = [&](const uint32_t (&v)[32], int ch) {
+        if (!stores) return;
         const int nvalid = t.nrows - ch * 32;
         const size_t row0 = (size_t)(t.r0 + ch * 32);
         if (MODE == MODE_UP) {
@@ -944,7 +995,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         // no chunk of this tile for this warp: the accumulator is free as far as it goes
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(acc ? tempty1 : tempty0);
-      } else if (pieces < 2) {
+      } else if (pieces < 2 || !stores) {
         for (int ch = h; ch < nch; ch += 2) {
           uint32_t v[32];
           tmem_ld_32cols(tb + ch * 32, v);
@@ -1162,6 +1213,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   // small batches: every weight tile is read by one CTA pair, while the token rows and outputs are
   // read again by the next stage (x_perm / h / y_perm fit in L2)
   prm.l2_hints = (a.mode != MODE_GATE && a.T <= kL2HintMaxTokens) ? 1 : 0;
+  prm.offsets_early = a.mode != MODE_GATE ? a.offsets_early : 0;
   if (a.mode != MODE_GATE && a.sched != nullptr) {
     prm.split_part = a.split_part;
     prm.split_cnt = a.split_cnt;

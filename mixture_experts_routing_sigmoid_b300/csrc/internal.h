@@ -159,6 +159,9 @@ struct GemmArgs {
                             // split along K (kSplitMaxPieces pieces), or nullptr (no split)
   int* split_cnt;           // UP / DOWN: kSplitCounters arrival counters of those pieces, zero
                             // at launch (the last arrival sets its counter back to zero)
+  int offsets_early;        // UP / DOWN: 1 when `offsets` were written by a kernel at least two
+                            // launches back in the stream (or before a non-kernel node), so the
+                            // GEMM may read them before waiting for the kernel just ahead
   int* err;
 };
 // Tail split of the expert GEMMs: tiles of the last, partly filled wave are cut along K into
