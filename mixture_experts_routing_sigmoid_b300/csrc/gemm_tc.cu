@@ -615,7 +615,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   for (int q = threadIdx.x; q < nprob; q += THREADS) {
     const uint32_t kq = c.key[q];
     int rank = 0;
-    for (int o = 0; o < nprob; o += 4) {  // four keys per shared load
+#pragma unroll 8
+    for (int o = 0; o < nprob; o += 4) {  // four keys per shared load, loads overlapped
       const uint4 k4 = *reinterpret_cast<const uint4*>(&c.key[o]);
       rank += (k4.x > kq) + (k4.y > kq) + (k4.z > kq) + (k4.w > kq);
     }
@@ -1156,8 +1157,9 @@ bool make_token_maps(CUtensorMap* big, CUtensorMap* small, const void* base, uin
   return make_map(big, base, inner, outer, XBOX_L) && make_map(small, base, inner, outer, XBOX_S);
 }
 
+// max_pairs > 0 caps the grid at that many CTA pairs.
 template <int MODE, int NS>
-cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
+cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st, int max_pairs = 0) {
   static int grid_for_device[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1190,6 +1192,7 @@ cudaError_t launch_mode(const TcParams& prm, int num_sms, cudaStream_t st) {
     grid = 2 * (clusters < num_sms / 2 ? clusters : num_sms / 2);
     if (dev >= 0 && dev < 64) grid_for_device[dev] = grid;
   }
+  if (max_pairs > 0 && 2 * max_pairs < grid) grid = 2 * max_pairs;
   cfg.gridDim = dim3(grid, 1, 1);
   note_launches(1);
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, NS>, prm);
@@ -1244,7 +1247,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
         prm.gate_part = a.gate_part;
       }
     }
-    cudaError_t e = launch_mode<MODE_GATE, 3>(prm, num_sms, st);
+    // one pair per work item (the items are fewer than the pairs whenever K is split)
+    const int items = tiles * prm.splits;
+    cudaError_t e = launch_mode<MODE_GATE, 3>(prm, num_sms, st, items < pairs ? items : 0);
     if (e != cudaSuccess || prm.splits == 1) return e;
     int blocks = (int)(((size_t)T * N + 255) / 256);
     if (blocks > num_sms * 8) blocks = num_sms * 8;
