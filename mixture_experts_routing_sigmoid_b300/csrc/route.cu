@@ -678,7 +678,13 @@ __device__ __noinline__ bool redo_fp64(const float* ut, const float* bias, bool 
   return sel.ok;
 }
 
-__global__ void __launch_bounds__(256) route_kernel(RouteArgs a) {
+// MINB: CTAs per SM the registers must allow. The calls to the exact recheck (rare: no token of
+// the V3 prefill batch takes it) make the compiler size the kernel for the recheck's registers
+// (123), two CTAs per SM; large batches, which need the warps to hide the loads, cap it at four
+// CTAs (64 registers; the recheck spills, measured 61.6 -> 54.6 us at 16384 tokens), while small
+// batches, where one warp's latency is the kernel's, keep the registers (8.0 vs 9.9 us at 512).
+template <int MINB>
+__global__ void __launch_bounds__(256, MINB) route_kernel(RouteArgs a) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int J = (a.N + 31) >> 5;
@@ -1061,13 +1067,16 @@ cudaError_t launch_group_losses(const GroupLossArgs& a, cudaStream_t st) {
   return e;
 }
 
+constexpr int kRouteWideMinTokens = 1024;  // batches above this use route_kernel<4>
+
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
   const int warps_needed = a.T;
   int blocks = (warps_needed + 7) / 8;
   const int cap = num_sms * 8;
   if (blocks > cap) blocks = cap;
-  return launch_pdl(route_kernel, dim3(blocks), dim3(256), 0, st, a);
+  return a.T > kRouteWideMinTokens ? launch_pdl(route_kernel<4>, dim3(blocks), dim3(256), 0, st, a)
+                                   : launch_pdl(route_kernel<1>, dim3(blocks), dim3(256), 0, st, a);
 }
 
 int stats_blocks(int T) {
