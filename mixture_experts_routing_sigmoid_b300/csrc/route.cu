@@ -94,8 +94,10 @@ struct FastSel {
 };
 
 // gj[j]: group of this lane's expert j*32 + lane; ok[j]: its ordered key (0: no expert).
-__device__ __forceinline__ FastSel fast_select(const uint32_t (&ok)[MAXJ], const float (&s)[MAXJ],
-                                               const int (&gj)[MAXJ], int lane, int K, int G,
+// JM: experts per lane the caller holds (a compile-time bound on ceil(N / 32)).
+template <int JM>
+__device__ __forceinline__ FastSel fast_select(const uint32_t (&ok)[JM], const float (&s)[JM],
+                                               const int (&gj)[JM], int lane, int K, int G,
                                                int Gk, int topn) {
   FastSel out;
   out.ok = true;
@@ -108,7 +110,7 @@ __device__ __forceinline__ FastSel fast_select(const uint32_t (&ok)[MAXJ], const
     for (int g = 0; g < G; ++g) {
       uint32_t l1 = 0, l2 = 0;
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j) {
+      for (int j = 0; j < JM; ++j) {
         if (gj[j] == g) {
           const uint32_t v = ok[j];
           if (v > l1) { l2 = l1; l1 = v; } else if (v > l2) { l2 = v; }
@@ -144,7 +146,7 @@ __device__ __forceinline__ FastSel fast_select(const uint32_t (&ok)[MAXJ], const
   }
   uint32_t avail = 0;  // bit j: expert j*32 + lane is eligible and not chosen yet
 #pragma unroll
-  for (int j = 0; j < MAXJ; ++j)
+  for (int j = 0; j < JM; ++j)
     if (ok[j] != 0u && gj[j] >= 0 && ((out.gmask >> gj[j]) & 1u)) avail |= 1u << j;
   out.e = -1;
   out.se = 0.0f;
@@ -156,7 +158,7 @@ __device__ __forceinline__ FastSel fast_select(const uint32_t (&ok)[MAXJ], const
     int bj = 0;
     float bs = 0.0f;
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j)
+    for (int j = 0; j < JM; ++j)
       if (((avail >> j) & 1u) && ok[j] > best) { best = ok[j]; bj = j; bs = s[j]; }
     const uint32_t m = __reduce_max_sync(FULL_MASK, best);
     if (r == K) {
@@ -683,7 +685,8 @@ __device__ __noinline__ bool redo_fp64(const float* ut, const float* bias, bool 
 // (123), two CTAs per SM; large batches, which need the warps to hide the loads, cap it at four
 // CTAs (64 registers; the recheck spills, measured 61.6 -> 54.6 us at 16384 tokens), while small
 // batches, where one warp's latency is the kernel's, keep the registers (8.0 vs 9.9 us at 512).
-template <int MINB>
+// JM: experts per lane, a compile-time bound on ceil(N / 32) (the launcher picks 2, 4, 5 or 8).
+template <int MINB, int JM>
 __global__ void __launch_bounds__(256, MINB) route_kernel(RouteArgs a) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -695,10 +698,10 @@ __global__ void __launch_bounds__(256, MINB) route_kernel(RouteArgs a) {
 
   pdl_wait();
   pdl_trigger();
-  float b[MAXJ];
-  int gj[MAXJ];
+  float b[JM];
+  int gj[JM];
 #pragma unroll
-  for (int j = 0; j < MAXJ; ++j) {
+  for (int j = 0; j < JM; ++j) {
     const int e = j * 32 + lane;
     const bool v = j < J && e < a.N;
     b[j] = (a.bias != nullptr && v) ? a.bias[e] : 0.0f;
@@ -707,30 +710,30 @@ __global__ void __launch_bounds__(256, MINB) route_kernel(RouteArgs a) {
 
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < a.T; t += warps) {
     const float* ut = a.u + (size_t)t * a.N;
-    float u[MAXJ];
+    float u[JM];
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) u[j] = gj[j] >= 0 ? ut[j * 32 + lane] : -INFINITY;
+    for (int j = 0; j < JM; ++j) u[j] = gj[j] >= 0 ? ut[j * 32 + lane] : -INFINITY;
     // ---- fp32 scores and keys
-    float s[MAXJ];
+    float s[JM];
     float umax = u[0];
 #pragma unroll
-    for (int j = 1; j < MAXJ; ++j) umax = fmaxf(umax, u[j]);
+    for (int j = 1; j < JM; ++j) umax = fmaxf(umax, u[j]);
     umax = warp_max(umax);
     if (sigmoid) {
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j) s[j] = 1.0f / (1.0f + expf(-u[j]));
+      for (int j = 0; j < JM; ++j) s[j] = 1.0f / (1.0f + expf(-u[j]));
     } else {
       float z = 0.0f;
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j) { s[j] = expf(u[j] - umax); z += s[j]; }
+      for (int j = 0; j < JM; ++j) { s[j] = expf(u[j] - umax); z += s[j]; }
       z = warp_sum(z);
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j) s[j] = s[j] / z;
+      for (int j = 0; j < JM; ++j) s[j] = s[j] / z;
     }
-    uint32_t ok[MAXJ];
+    uint32_t ok[JM];
     float kmax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) {
+    for (int j = 0; j < JM; ++j) {
       const float key = logit_keys ? u[j] : s[j] + b[j];
       ok[j] = gj[j] >= 0 ? ord32(key) : 0u;
       if (gj[j] >= 0) kmax = fmaxf(kmax, fabsf(key));
@@ -763,7 +766,7 @@ __global__ void __launch_bounds__(256, MINB) route_kernel(RouteArgs a) {
         const int e = __shfl_sync(FULL_MASK, sel_e, r);
         float mine = 0.0f;
 #pragma unroll
-        for (int j = 0; j < MAXJ; ++j)
+        for (int j = 0; j < JM; ++j)
           if (e == j * 32 + lane) mine = s[j];
         const float v = __shfl_sync(FULL_MASK, mine, e & 31);
         if (lane == r) sel_s = v;
@@ -778,7 +781,7 @@ __global__ void __launch_bounds__(256, MINB) route_kernel(RouteArgs a) {
       double z = 0.0;
       if (!sigmoid) {
 #pragma unroll
-        for (int j = 0; j < MAXJ; ++j)
+        for (int j = 0; j < JM; ++j)
           z += gj[j] >= 0 ? exp((double)u[j] - (double)umax) : 0.0;
         z = warp_sum(z);
       }
@@ -788,7 +791,7 @@ __global__ void __launch_bounds__(256, MINB) route_kernel(RouteArgs a) {
         const int er = __shfl_sync(FULL_MASK, sel_e, r);
         float mine = 0.0f;
 #pragma unroll
-        for (int j = 0; j < MAXJ; ++j)
+        for (int j = 0; j < JM; ++j)
           if (er == j * 32 + lane) mine = u[j];
         const float v = __shfl_sync(FULL_MASK, mine, er & 31);
         if (lane == r) ul = v;
@@ -838,6 +841,7 @@ struct Kahan {
 // each): the scores of every expert, lse and lse^2, and (with part_c) the assignment counts.
 constexpr int STATS_TOK_PER_WARP = 2;
 constexpr int STATS_THREADS = 256;
+template <int JM>  // experts per lane (a compile-time bound on ceil(N / 32))
 __global__ void __launch_bounds__(STATS_THREADS) stats_partial_kernel(StatsArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -850,15 +854,15 @@ __global__ void __launch_bounds__(STATS_THREADS) stats_partial_kernel(StatsArgs 
   if (a.part_c != nullptr)
     for (int e = threadIdx.x; e < 256; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
-  float acc[MAXJ];
+  float acc[JM];
 #pragma unroll
-  for (int j = 0; j < MAXJ; ++j) acc[j] = 0.0f;
+  for (int j = 0; j < JM; ++j) acc[j] = 0.0f;
   float l1 = 0.0f, l2 = 0.0f;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < a.T; t += warps) {
     const float* ut = a.u + (size_t)t * a.N;
-    float u[MAXJ];
+    float u[JM];
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) {
+    for (int j = 0; j < JM; ++j) {
       const int e = j * 32 + lane;
       u[j] = (j < J && e < a.N) ? ut[e] : -INFINITY;
     }
@@ -869,26 +873,26 @@ __global__ void __launch_bounds__(STATS_THREADS) stats_partial_kernel(StatsArgs 
     }
     float m = u[0];
 #pragma unroll
-    for (int j = 1; j < MAXJ; ++j) m = fmaxf(m, u[j]);
+    for (int j = 1; j < JM; ++j) m = fmaxf(m, u[j]);
     m = warp_max(m);
-    float ex[MAXJ], z = 0.0f;
+    float ex[JM], z = 0.0f;
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) { ex[j] = expf(u[j] - m); z += ex[j]; }
+    for (int j = 0; j < JM; ++j) { ex[j] = expf(u[j] - m); z += ex[j]; }
     z = warp_sum(z);
     if (a.score_fn == 1) {
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j)
+      for (int j = 0; j < JM; ++j)
         if (j < J && j * 32 + lane < a.N) acc[j] += 1.0f / (1.0f + expf(-u[j]));
     } else {
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j) acc[j] += ex[j] / z;
+      for (int j = 0; j < JM; ++j) acc[j] += ex[j] / z;
     }
     const float lse = m + logf(z);
     l1 += lse;
     l2 += lse * lse;
   }
 #pragma unroll
-  for (int j = 0; j < MAXJ; ++j) {
+  for (int j = 0; j < JM; ++j) {
     const int e = j * 32 + lane;
     if (e < 256) red[wid][e] = (j < J && e < a.N) ? acc[j] : 0.0f;
   }
@@ -1054,6 +1058,23 @@ __global__ void __launch_bounds__(256) group_final_kernel(GroupLossArgs a) {
 
 }  // namespace
 
+// The instantiation whose experts-per-lane bound JM covers ceil(N / 32) with the least waste.
+template <int MINB>
+cudaError_t launch_route_jm(const RouteArgs& a, dim3 grid, cudaStream_t st) {
+  const int J = (a.N + 31) >> 5;
+  if (J <= 2) return launch_pdl(route_kernel<MINB, 2>, grid, dim3(256), 0, st, a);
+  if (J <= 4) return launch_pdl(route_kernel<MINB, 4>, grid, dim3(256), 0, st, a);
+  if (J <= 5) return launch_pdl(route_kernel<MINB, 5>, grid, dim3(256), 0, st, a);
+  return launch_pdl(route_kernel<MINB, 8>, grid, dim3(256), 0, st, a);
+}
+cudaError_t launch_stats_partial(const StatsArgs& a, dim3 grid, cudaStream_t st) {
+  const int J = (a.N + 31) >> 5;
+  if (J <= 2) return launch_pdl(stats_partial_kernel<2>, grid, dim3(STATS_THREADS), 0, st, a);
+  if (J <= 4) return launch_pdl(stats_partial_kernel<4>, grid, dim3(STATS_THREADS), 0, st, a);
+  if (J <= 5) return launch_pdl(stats_partial_kernel<5>, grid, dim3(STATS_THREADS), 0, st, a);
+  return launch_pdl(stats_partial_kernel<8>, grid, dim3(STATS_THREADS), 0, st, a);
+}
+
 cudaError_t launch_group_losses(const GroupLossArgs& a, cudaStream_t st) {
   if (a.st.T <= 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(a.st.counts, 0, sizeof(int32_t) * a.st.N, st);
@@ -1062,12 +1083,12 @@ cudaError_t launch_group_losses(const GroupLossArgs& a, cudaStream_t st) {
   int cb = (a.st.T + 255) / 256;
   if (cb > 1184) cb = 1184;
   e = launch_pdl(group_count_kernel, dim3(cb), dim3(256), 0, st, a);
-  if (e == cudaSuccess) e = launch_pdl(stats_partial_kernel, dim3(a.st.nblk), dim3(256), 0, st, a.st);
+  if (e == cudaSuccess) e = launch_stats_partial(a.st, dim3(a.st.nblk), st);
   if (e == cudaSuccess) e = launch_pdl(group_final_kernel, dim3(1), dim3(256), 0, st, a);
   return e;
 }
 
-constexpr int kRouteWideMinTokens = 1024;  // batches above this use route_kernel<4>
+constexpr int kRouteWideMinTokens = 1024;  // batches above this use route_kernel<4, *>
 
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
@@ -1075,8 +1096,8 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   int blocks = (warps_needed + 7) / 8;
   const int cap = num_sms * 8;
   if (blocks > cap) blocks = cap;
-  return a.T > kRouteWideMinTokens ? launch_pdl(route_kernel<4>, dim3(blocks), dim3(256), 0, st, a)
-                                   : launch_pdl(route_kernel<1>, dim3(blocks), dim3(256), 0, st, a);
+  return a.T > kRouteWideMinTokens ? launch_route_jm<4>(a, dim3(blocks), st)
+                                   : launch_route_jm<1>(a, dim3(blocks), st);
 }
 
 int stats_blocks(int T) {
@@ -1088,7 +1109,7 @@ int stats_blocks(int T) {
 
 cudaError_t launch_stats(const StatsArgs& a, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(stats_partial_kernel, dim3(a.nblk), dim3(STATS_THREADS), 0, st, a);
+  cudaError_t e = launch_stats_partial(a, dim3(a.nblk), st);
   if (e == cudaSuccess)
     e = launch_pdl(stats_final_kernel, dim3(1), dim3(STATS_FINAL_THREADS), 0, st, a);
   return e;
