@@ -171,31 +171,36 @@ __global__ void __launch_bounds__(PB) perm_hist_kernel(PermuteArgs p) {
 __global__ void __launch_bounds__(256) perm_scan_kernel(PermuteArgs p, int nb) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int tot[256];
-  __shared__ int excl[257];
-  const int e = threadIdx.x;
+  __shared__ int wtot[8];
+  const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
+  // base[b][e]: expert e's rows in the blocks before b (the scatter adds the expert's offset);
+  // eight blocks' counts are loaded before they are added
   int running = 0;
   if (e < p.N) {
-    for (int b = 0; b < nb; ++b) {
-      const int c = p.cnt[(size_t)b * p.N + e];
-      p.base[(size_t)b * p.N + e] = running;
-      running += c;
+    for (int b0 = 0; b0 < nb; b0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = b0 + i < nb ? p.cnt[(size_t)(b0 + i) * p.N + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (b0 + i < nb) p.base[(size_t)(b0 + i) * p.N + e] = running;
+        running += c[i];
+      }
     }
   }
-  tot[e] = (e < p.N) ? running : 0;
-  __syncthreads();
-  if (e == 0) {
-    int acc = 0;
-    for (int i = 0; i < p.N; ++i) { excl[i] = acc; acc += tot[i]; }
-    excl[p.N] = acc;
+  // exclusive scan of the experts' totals: warp scans, then the warp totals
+  int incl = e < p.N ? running : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += v;
   }
+  if (lane == 31) wtot[wid] = incl;
   __syncthreads();
-  if (e < p.N) {
-    const int off = excl[e];
-    p.offsets[e] = off;
-    for (int b = 0; b < nb; ++b) p.base[(size_t)b * p.N + e] += off;
-  }
-  if (e == 0) p.offsets[p.N] = excl[p.N];
+  int before = 0;
+  for (int w = 0; w < wid; ++w) before += wtot[w];
+  if (e < p.N) p.offsets[e] = before + incl - running;
+  if (e == p.N - 1) p.offsets[p.N] = before + incl;
   if (blockIdx.x == 0 && p.sched_zero != nullptr)
     for (int i = e; i < kSchedInts; i += blockDim.x) p.sched_zero[i] = 0;
 }
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(PB) perm_scatter_kernel(PermuteArgs p) {
     const uint32_t* m = p.masks + ((size_t)blockIdx.x * p.N + e) * 8;
     int rank = __popc(m[wi] & below);
     for (int i = 0; i < wi; ++i) rank += __popc(m[i]);
-    const int row = p.base[(size_t)blockIdx.x * p.N + e] + rank;
+    const int row = p.offsets[e] + p.base[(size_t)blockIdx.x * p.N + e] + rank;
     p.slot_row[a] = row;
     p.row_token[row] = t;
     if (p.row_w != nullptr) p.row_w[row] = p.w[a];

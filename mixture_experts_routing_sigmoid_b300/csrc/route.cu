@@ -912,17 +912,39 @@ __global__ void __launch_bounds__(STATS_THREADS) stats_partial_kernel(StatsArgs 
   }
 }
 
-// Tree sum over the 1024 threads of a block in a fixed order (every thread gets the result).
-__device__ __forceinline__ float block_sum_1024(float v, float* sh) {
-  sh[threadIdx.x] = v;
-  __syncthreads();
-  for (int o = 512; o > 0; o >>= 1) {
-    if ((int)threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
-    __syncthreads();
+// Sums of NV values over the 1024 threads of a block, each in a fixed order (a shuffle tree in
+// every warp, then one over the 32 warp sums); every thread gets the results. sh: [32][NV].
+template <int NV>
+__device__ __forceinline__ void block_sums_1024(float (&v)[NV], float (*sh)[NV]) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[i] += __shfl_down_sync(FULL_MASK, v[i], o);
   }
-  const float r = sh[0];
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) sh[wid][i] = v[i];
+  }
   __syncthreads();
-  return r;
+  if (wid == 0) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      float x = sh[lane][i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(FULL_MASK, x, o);
+      v[i] = x;
+    }
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) sh[0][i] = v[i];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = sh[0][i];
+  __syncthreads();
 }
 
 // Fixed-order reduction of the partials: counts, f, P, L_B, L_Z, mean lse. Q = 1024 / N' threads
@@ -979,7 +1001,11 @@ __global__ void __launch_bounds__(STATS_FINAL_THREADS) stats_final_kernel(StatsA
     if (a.part_c == nullptr) count = a.counts[e];
   }
   __syncthreads();
-  const float total = block_sum_1024(q == 0 ? colsum : 0.0f, tree);
+  // the column total and the two lse sums in one pass, then L_B's sum
+  __shared__ float sums[32][3];
+  float r3[3] = {q == 0 ? colsum : 0.0f, s1.s, s2.s};
+  block_sums_1024<3>(r3, sums);
+  const float total = r3[0], l1 = r3[1], l2 = r3[2];
   float fe = 0.0f, pe = 0.0f;
   if (q == 0 && e < a.N) {
     if (a.part_c != nullptr) a.counts[e] = count;
@@ -988,9 +1014,9 @@ __global__ void __launch_bounds__(STATS_FINAL_THREADS) stats_final_kernel(StatsA
     if (a.f) a.f[e] = fe;
     if (a.P) a.P[e] = pe;
   }
-  const float lb = block_sum_1024(fe * pe, tree);
-  const float l1 = block_sum_1024(s1.s, tree);
-  const float l2 = block_sum_1024(s2.s, tree);
+  float r1[1] = {fe * pe};
+  block_sums_1024<1>(r1, reinterpret_cast<float (*)[1]>(&sums[0][0]));
+  const float lb = r1[0];
   if (threadIdx.x == 0 && a.lb_z) {
     a.lb_z[0] = lb * a.N;
     a.lb_z[1] = l2 / a.T;
