@@ -20,7 +20,14 @@ ROUTE_CFGS = {**CONFIGS, "mid_a": MID_A, "mid_b": MID_B, "mid_v2": MID_V2, "mid_
                                            topk_groups=4, top_k=16, group_score_topn=2,
                                            score_fn="sigmoid", norm_topk=True,
                                            routed_scale=1.5, has_select_bias=True,
-                                           select_bias_std=0.05)}
+                                           select_bias_std=0.05),
+              # 128 experts: four per lane (the routing and statistics kernels' JM = 4 builds),
+              # at a batch above and one below the large-batch routing kernel's threshold
+              "n128": CONFIGS["v3_prefill"].replace(name="n128", T=2000, n_routed=128,
+                                                    n_groups=8, topk_groups=4, top_k=8),
+              "n128_small": CONFIGS["v3_prefill"].replace(name="n128_small", T=300,
+                                                          n_routed=128, n_groups=8,
+                                                          topk_groups=4, top_k=8)}
 
 
 def _oracle_route(cfg, u, sb):
@@ -82,7 +89,7 @@ def test_route_single_token_and_tail_sizes():
         _check_route(cfg, u, make_router(cfg)["select_bias"], f"T={T}")
 
 
-@pytest.mark.parametrize("name", ["tiny", "v1", "v2", "v3_prefill", "mid_a"])
+@pytest.mark.parametrize("name", ["tiny", "v1", "v2", "v3_prefill", "mid_a", "n128"])
 def test_load_stats(name):
     import mixture_experts_routing_sigmoid_b300 as moe
     cfg = ROUTE_CFGS[name]
