@@ -196,17 +196,6 @@ __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
-// 2D tiled load of a box into shared memory, completing `bytes` on mbarrier `bar`.
-// c0 = innermost (contiguous) coordinate in elements, c1 = row.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
-                                            int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
 // ------------------------------------------------------------------ tcgen05 / TMEM
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -294,17 +283,18 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
                :: "r"(cluster_addr) : "memory");
 }
-// 2D tiled TMA load into this CTA's shared memory whose completion is counted on an mbarrier
-// of either CTA of the pair (`bar_cluster`, a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
-                                                 uint32_t bar_cluster, int c0, int c1) {
+// 3D tiled TMA load (coordinates innermost first) into this CTA's shared memory whose completion
+// is counted on an mbarrier of either CTA of the pair (`bar_cluster`, a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1),
+         "r"(c2)
       : "memory");
 }
-// 5D tiled TMA load (coordinates innermost first), completion counted as for tma_load_2d_pair.
+// 5D tiled TMA load (coordinates innermost first), completion counted as for tma_load_3d_pair.
 __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const void* tmap,
                                                  uint32_t bar_cluster, int c0, int c1, int c2,
                                                  int c3, int c4) {
@@ -319,7 +309,7 @@ __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const void* tmap,
 // tensor whose map has a box one row high, columns c0 .. c0 + box width - 1, written as four
 // consecutive box rows at dst (the layout a 4-row tiled box would have there; with a swizzled
 // map the pattern follows the shared-memory address as for tiled loads). Completion counted as
-// for tma_load_2d_pair.
+// for tma_load_3d_pair.
 __device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const void* tmap,
                                                  uint32_t bar_cluster, int c0, int r0, int r1,
                                                  int r2, int r3) {
@@ -343,15 +333,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-// tma_load_2d_pair / tma_load_5d_pair with an L2 policy for the loaded lines.
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* tmap,
+// tma_load_3d_pair / tma_load_5d_pair with an L2 policy for the loaded lines.
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* tmap,
                                                       uint32_t bar_cluster, int c0, int c1,
-                                                      uint64_t policy) {
+                                                      int c2, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;"
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1),
-         "l"(policy)
+         "r"(c2), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_5d_pair_hint(uint32_t dst, const void* tmap,

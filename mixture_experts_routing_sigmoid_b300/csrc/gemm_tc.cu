@@ -37,11 +37,14 @@
 // (Claiming later, a few k blocks before the current tile's end, measured 1.5-3% slower.)
 //   warp 0      TMA producer (both CTAs): this CTA's weight rows and token rows of one k block
 //               per stage, in a 200 KB ring of stages sized by the tile (below). A k block is
-//               128 elements, two 128-byte-swizzled units of 64 (one TMA box per operand and
-//               unit); when K / 64 is odd the last block holds one unit. Two units per stage
-//               halve the barrier round trips per FLOP against one-unit stages.
-//               Completion of both CTAs' loads is counted on the first CTA's full barrier; the
-//               MMA's commit frees the stage in both CTAs.
+//               128 elements, two 128-byte-swizzled units of 64, and each operand's two units
+//               come in one TMA box (when K / 64 is odd the last block's second unit lies past
+//               the end and reads as zeros). Two units per stage halve the barrier round trips
+//               per FLOP against one-unit stages; one copy per operand and stage keeps the
+//               producer's time per stage, which bounds how fast a tile with few tokens can
+//               stream its weights, to about half of what a copy per unit and token box took.
+//               Lane 0 alone walks a tile's stages. Completion of both CTAs' loads is counted
+//               on the first CTA's full barrier; the MMA's commit frees the stage in both CTAs.
 //   warp 1      TMEM owner (both CTAs) and, in the first CTA, MMA issuer: a single thread waits
 //               for each stage and issues its tcgen05.mma (M=256, N=tile's tokens rounded up to
 //               16, K=16; four per unit) into one of two 256-column fp32 accumulators.
@@ -76,7 +79,7 @@ constexpr int EPI_WARPS = 8;             // warps 2 .. 9
 constexpr int SCHED_WARP = 10;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;       // two accumulators
-constexpr int XBOX_S = 32, XBOX_L = 64;  // token rows per TMA box (small / large map)
+constexpr int NTOKMAP = 3;               // token maps: boxes of 32, 64 or 128 rows
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;    // 2 s per wait
 constexpr unsigned long long GRACE_NS = 100000000ull;       // drain after an abort
 
@@ -104,10 +107,14 @@ constexpr int NSLOT = 6;                 // more than the stages that fit at onc
 constexpr int kDeepRingMaxTokens = 512;
 constexpr int kGateMaxSplits = 16;
 
+// Every stage is filled by one weight copy and one token copy per CTA: the maps view K as
+// (64-element unit, chunk of 64 units...) so that one box spans both k units of a stage (a TMA
+// instruction costs the issuing thread on the order of a hundred cycles whatever its box, and
+// the producer's per-stage time bounds the weight stream of a tile with few tokens).
 struct TcParams {
-  CUtensorMap tmW0, tmW1;    // weights: routed, shared (box 128 rows; UP: interleaved 5-D box)
-  CUtensorMap tmX0, tmX1;    // tokens: routed, shared (box 64 rows)
-  CUtensorMap tmX0s, tmX1s;  // tokens: routed, shared (box 32 rows)
+  CUtensorMap tmW0, tmW1;    // weights: routed, shared (128 rows x 2 units; UP: interleaved 5-D)
+  CUtensorMap tmX0[NTOKMAP]; // tokens, routed: 32, 64 or 128 rows x 2 units
+  CUtensorMap tmX1[NTOKMAP]; // tokens, shared
   CUtensorMap tmXg;          // UP with row gather: x [T, H], box one row high (tile::gather4)
   const int32_t* row_token;  // UP with row gather: token of each routed row, else nullptr
   const int32_t* offsets;
@@ -139,8 +146,8 @@ struct alignas(16) Tile {
   int r0;        // first token row (in the problem's activation tensor)
   int nrows;     // token rows of this tile that are stored
   int ncols;     // MMA N: nrows rounded up to 16; each CTA holds ncols / 2 token rows
-  int nbox;      // token boxes loaded per CTA and stage
-  int big_box;   // boxes of 64 rows (else one box of 32)
+  int tok_rows;  // token rows per CTA and unit in a stage: 32, 64 or 128 (>= ncols / 2)
+  int tsel;      // its token map: 0, 1, 2
   int ku0, ku;   // first k unit and k units (GATE split-K: this split's range)
   int kb;        // k blocks (stages): ku / UNITS rounded up
   int split;     // GATE split-K: which split. UP / DOWN: piece | pieces << 8 | split tile << 16
@@ -233,8 +240,8 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const SmemCtl& c,
   t.nrows = min(per, rows - tt * per);
   t.ncols = (t.nrows + 15) & ~15;
   const int half = t.ncols / 2;
-  t.big_box = half > XBOX_S ? 1 : 0;
-  t.nbox = t.big_box ? (half + XBOX_L - 1) / XBOX_L : 1;
+  t.tsel = half <= 32 ? 0 : (half <= 64 ? 1 : 2);
+  t.tok_rows = 32 << t.tsel;
   t.ku0 = 0;
   t.ku = k_units_of<MODE>(p, t.shared);
   if (MODE == MODE_GATE && p.splits > 1) {
@@ -283,11 +290,12 @@ __device__ __forceinline__ Tile decode_item(const TcParams& p, const SmemCtl& c,
   return t;
 }
 
-// Bytes of one unit of this CTA's token rows in a stage of tile t: the boxes it loads, or with
-// the row gather its rows (a multiple of 8 rows: 1 KB aligned, as the 128-byte swizzle wants).
+// Bytes of one unit of this CTA's token rows in a stage of tile t: the box rows it loads, or
+// with the row gather its rows (a multiple of 8 rows: 1 KB aligned, as the 128-byte swizzle
+// wants).
 __device__ __forceinline__ uint32_t tok_unit_bytes(const Tile& t, bool gathered) {
   if (gathered) return (uint32_t)(t.ncols / 2) * KU * 2;
-  return (uint32_t)t.nbox * (t.big_box ? XBOX_L : XBOX_S) * KU * 2;
+  return (uint32_t)t.tok_rows * KU * 2;
 }
 __device__ __forceinline__ uint32_t stage_bytes_of(const Tile& t, bool gathered) {
   return A_BYTES + UNITS * tok_unit_bytes(t, gathered);
@@ -337,48 +345,36 @@ __device__ __forceinline__ Tile end_tile() {
   return t;
 }
 
-// Coordinates of this CTA's boxes for k unit ku of tile t: the weight box at (ax, ay0) (UP:
-// 5-D coordinates (ax, 0, 0, ay0 = first 16-feature group, ay1 = expert)); token boxes at
-// (bx, by0 + box_rows j), j < t.nbox.
-struct Boxes {
+// This CTA's copies for tile t, fixed along K: the weight map and box (UP: 5-D coordinates
+// (0, 0, wa = 2 * expert, wb = first 16-feature group, chunk); else 3-D (0, wa = row, chunk))
+// and the token map and first row (3-D (0, trow, chunk)). The chunk coordinate is the stage's
+// first k unit; one box brings that unit and the next.
+struct TileBoxes {
   const CUtensorMap* tw;
   const CUtensorMap* tx;
-  int ax, ay0, ay1, bx, by0, box_rows, box_bytes;
+  int wa, wb, trow;
 };
 
 template <int MODE>
-__device__ __forceinline__ Boxes boxes_of(const TcParams& p, const Tile& t, int ku, uint32_t rank) {
-  Boxes b;
+__device__ __forceinline__ TileBoxes tile_boxes(const TcParams& p, const Tile& t, uint32_t rank) {
+  TileBoxes b;
   b.tw = t.shared ? &p.tmW1 : &p.tmW0;
-  if (t.big_box) {
-    b.tx = t.shared ? &p.tmX1 : &p.tmX0;
-    b.box_rows = XBOX_L;
-  } else {
-    b.tx = t.shared ? &p.tmX1s : &p.tmX0s;
-    b.box_rows = XBOX_S;
-  }
-  b.box_bytes = b.box_rows * KU * 2;
-  const int k0 = ku * KU;
-  b.ax = k0;
-  b.ay1 = 0;
+  b.tx = t.shared ? &p.tmX1[t.tsel] : &p.tmX0[t.tsel];
   int fc = t.f0 + (int)rank * feat_per_cta<MODE>();    // this CTA's first feature
   if (fc >= feat_total<MODE>(p, t.shared)) fc = t.f0;  // past the end: recompute CTA 0's rows
+  b.wb = 0;
   if (MODE == MODE_UP) {
     const int s = fc / p.I, j = fc - s * p.I;          // expert (shared: stacked), feature in it
-    b.ay0 = j / 16;
-    b.ay1 = t.shared ? s : t.prob;
+    b.wa = 2 * (t.shared ? s : t.prob);
+    b.wb = j / 16;
   } else if (MODE == MODE_DOWN) {
-    if (!t.shared) {
-      b.ay0 = t.prob * p.H + fc;
-    } else {
-      b.ax = k0 % p.I;
-      b.ay0 = (k0 / p.I) * p.H + fc;
-    }
+    // shared: the k range runs over the shared experts' stacked intermediate sizes; the
+    // stage's expert adds its H rows (see the producer)
+    b.wa = t.shared ? fc : t.prob * p.H + fc;
   } else {
-    b.ay0 = fc;
+    b.wa = fc;
   }
-  b.bx = k0;
-  b.by0 = t.r0 + (int)rank * (t.ncols / 2);
+  b.trow = t.r0 + (int)rank * (t.ncols / 2);
   return b;
 }
 
@@ -528,14 +524,11 @@ __device__ __forceinline__ bool ring_take(SmemCtl& c, uint32_t qs, uint32_t qph,
   return true;
 }
 
-// Warp-wide ring_take: lane 0 waits, every lane reads the slot, lane 0 releases it. With
-// `rows`, lane l also takes gathered rows 4l .. 4l+3 of the slot.
+// Warp-wide ring_take: lane 0 waits, every lane reads the slot, lane 0 releases it.
 __device__ __forceinline__ bool ring_take_warp(SmemCtl& c, uint32_t qs, uint32_t qph, Tile& t,
-                                               volatile int* abort_flag, int* err,
-                                               int4* rows = nullptr) {
+                                               volatile int* abort_flag, int* err) {
   if (!warp_wait_bounded(smem_u32(&c.lfull[qs]), qph, abort_flag, err, TIMEOUT_NS)) return false;
   lds_tile(smem_u32(&c.lsq[qs]), t);
-  if (rows != nullptr) *rows = *reinterpret_cast<const int4*>(&c.grow[qs][4 * (threadIdx.x & 31)]);
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&c.lempty[qs]));
   return true;
@@ -676,168 +669,158 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    const bool gather = MODE == MODE_UP && p.row_token != nullptr;
+    // Lane 0 alone: no warp-wide step between two stages (a shuffle or warp barrier there
+    // costs the stream of a tile with few tokens more than its copies do).
     if (lane == 0) {
+      const bool gather = MODE == MODE_UP && p.row_token != nullptr;
       tma_prefetch_desc(&p.tmW0);
       if (gather) {
         tma_prefetch_desc(&p.tmXg);
       } else {
-        tma_prefetch_desc(&p.tmX0);
-        tma_prefetch_desc(&p.tmX0s);
+#pragma unroll
+        for (int i = 0; i < NTOKMAP; ++i) tma_prefetch_desc(&p.tmX0[i]);
       }
       if (MODE != MODE_GATE && p.has_shared) {
         tma_prefetch_desc(&p.tmW1);
-        tma_prefetch_desc(&p.tmX1);
-        tma_prefetch_desc(&p.tmX1s);
-      }
-    }
-    const bool hint = p.l2_hints != 0;
-    const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
-    uint32_t seq = 0;                           // stages issued so far
-    RingPlace place;
-    uint32_t hlo[NS - 1], hhi[NS - 1];          // ring bytes of stages seq-1, seq-2, ...
 #pragma unroll
-    for (int i = 0; i < NS - 1; ++i) hlo[i] = hhi[i] = 0;
-    uint32_t issued_mask = 0, last_parity = 0;  // per slot: issued at least once / its parity
-    uint32_t qs = 0, qph = 0;                   // schedule ring slot and phase
-    bool ok = true;
-    // Places stage `seq` (`bytes` long) and names the stage whose release it must wait for:
-    // the latest earlier stage whose bytes it overlaps, or the barrier slot's previous stage
-    // (the MMA commits stages in order, so that one release covers every earlier stage).
-    auto plan = [&](uint32_t bytes, uint32_t& off, uint32_t& slot, int& w) {
-      off = place.place(bytes);
-      w = (int)seq - NS;
-#pragma unroll
-      for (int i = 0; i < NS - 1; ++i) {
-        const int j = (int)seq - 1 - i;
-        if (j > w && off < hhi[i] && hlo[i] < off + bytes) w = j;
+        for (int i = 0; i < NTOKMAP; ++i) tma_prefetch_desc(&p.tmX1[i]);
       }
+      const bool hint = p.l2_hints != 0;
+      const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
+      uint32_t seq = 0;                           // stages issued so far
+      RingPlace place;
+      uint32_t hlo[NS - 1], hhi[NS - 1];          // ring bytes of stages seq-1, seq-2, ...
 #pragma unroll
-      for (int i = NS - 2; i > 0; --i) { hlo[i] = hlo[i - 1]; hhi[i] = hhi[i - 1]; }
-      hlo[0] = off;
-      hhi[0] = off + bytes;
-      slot = seq % NS;
-    };
-    auto released = [&](int w) -> bool {
-      if (w < 0) return true;
-      return warp_wait_bounded(bar(c.empty[(uint32_t)w % NS]), ((uint32_t)w / NS) & 1u,
-                               abort_flag, p.err, TIMEOUT_NS);
-    };
-    auto issued = [&](uint32_t slot) {
-      issued_mask |= 1u << slot;
-      last_parity = (last_parity & ~(1u << slot)) | (((seq / NS) & 1u) << slot);
-      ++seq;
-    };
-    while (ok) {
-      Tile t;
-      int4 rows;  // row gather: this lane's four x rows
-      if (!ring_take_warp(c, qs, qph, t, abort_flag, p.err, gather ? &rows : nullptr)) {
-        ok = false;
-        break;
-      }
-      if (++qs == SQ) { qs = 0; qph ^= 1u; }
-      if (t.prob < 0) break;
-      if (rank == 0 && lane == 0) mbar_arrive(bar(c.took));  // the scheduler may claim the next
-      if (gather && !t.shared) {
-        // routed rows gathered from x: lanes 0 / 1 load the weight box of unit 0 / 1, lane l
-        // the x rows 4l .. 4l+3 of this CTA's half of the tile (one gather4 per unit)
-        const int half = t.ncols / 2;
-        const uint32_t tok_bytes = tok_unit_bytes(t, true);
-        const uint32_t sbytes = stage_bytes_of(t, true);
-        for (int kb = 0; kb < t.kb; ++kb) {
-          const int nu = min(UNITS, t.ku - kb * UNITS);
-          const int uw = lane & 1;
-          const Boxes b = boxes_of<MODE>(p, t, t.ku0 + kb * UNITS + uw, rank);
-          const int kx = (t.ku0 + kb * UNITS) * KU;
-          const uint32_t tx = 2 * nu * (A_UNIT + tok_bytes);
-          uint32_t off, slot;
-          int w;
-          plan(sbytes, off, slot, w);
-          const uint32_t fb = mapa_shared(bar(c.full[slot]), 0);
-          const uint32_t sa = sbase + off + uw * A_UNIT;
-          const uint32_t sg = sbase + off + A_BYTES + lane * (4 * KU * 2);
-          ready_before(fb); ready_before(sa); ready_before(sg); ready_before(tx);
-          ready_before(b.tw); ready_before((uint32_t)b.ax); ready_before((uint32_t)b.ay0);
-          ready_before((uint32_t)b.ay1); ready_before((uint32_t)kx);
-          if (!released(w)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[slot]), tx);
-          __syncwarp();
-          if (lane < nu) {
-            if (hint) tma_load_5d_pair_hint(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1, pol_w);
-            else tma_load_5d_pair(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1);
-          }
-          if (4 * lane < half) {
-            tma_gather4_pair(sg, &p.tmXg, fb, kx, rows.x, rows.y, rows.z, rows.w);
-            if (nu > 1)
-              tma_gather4_pair(sg + tok_bytes, &p.tmXg, fb, kx + KU, rows.x, rows.y, rows.z,
-                               rows.w);
-          }
-          __syncwarp();
-          issued(slot);
+      for (int i = 0; i < NS - 1; ++i) hlo[i] = hhi[i] = 0;
+      uint32_t issued_mask = 0, last_parity = 0;  // per slot: issued at least once / its parity
+      uint32_t qs = 0, qph = 0;                   // schedule ring slot and phase
+      bool ok = true;
+      // Places stage `seq` (`bytes` long) and waits for the release of the stage it must
+      // follow: the latest earlier stage whose bytes it overlaps, or the barrier slot's previous
+      // stage (the MMA commits stages in order, so that one release covers every earlier one).
+      auto place_and_wait = [&](uint32_t bytes, uint32_t& off, uint32_t& slot) -> bool {
+        off = place.place(bytes);
+        int w = (int)seq - NS;
+#pragma unroll
+        for (int i = 0; i < NS - 1; ++i) {
+          const int j = (int)seq - 1 - i;
+          if (j > w && off < hhi[i] && hlo[i] < off + bytes) w = j;
         }
-        continue;
-      }
-      const uint32_t tok_bytes = tok_unit_bytes(t, false);
-      const uint32_t sbytes = stage_bytes_of(t, false);
-      for (int kb = 0; kb < t.kb; ++kb) {
-        // everything the stage's copies need is computed before waiting for the slot
-        const int nu = min(UNITS, t.ku - kb * UNITS);             // units in this block
-        // lanes 0..7 serve unit 0, lanes 8..15 unit 1: lane 8u loads the weight box, lanes
-        // 8u + j (j < nbox) the token boxes
-        const int u = (lane >> 3) & 1, j = lane & 7;
-        const bool active = lane < 8 * nu;
-        const Boxes b = boxes_of<MODE>(p, t, t.ku0 + kb * UNITS + u, rank);
-        const uint32_t tx = 2 * nu * (A_UNIT + tok_bytes);
-        uint32_t off, slot;
-        int w;
-        plan(sbytes, off, slot, w);
-        const uint32_t fb = mapa_shared(bar(c.full[slot]), 0);  // the first CTA's barrier
-        const uint32_t sa = sbase + off + u * A_UNIT;
-        const uint32_t sb = sbase + off + A_BYTES + u * tok_bytes + j * b.box_bytes;
-        const int by = b.by0 + j * b.box_rows;
-        ready_before(fb); ready_before(sa); ready_before(sb); ready_before(tx);
-        ready_before(b.tw); ready_before(b.tx); ready_before((uint32_t)b.ax);
-        ready_before((uint32_t)b.ay0); ready_before((uint32_t)b.ay1);
-        ready_before((uint32_t)b.bx); ready_before((uint32_t)by);
-        if (!released(w)) {
+#pragma unroll
+        for (int i = NS - 2; i > 0; --i) { hlo[i] = hlo[i - 1]; hhi[i] = hhi[i - 1]; }
+        hlo[0] = off;
+        hhi[0] = off + bytes;
+        slot = seq % NS;
+        if (w < 0) return true;
+        return mbar_wait_bounded(bar(c.empty[(uint32_t)w % NS]), ((uint32_t)w / NS) & 1u,
+                                 abort_flag, p.err, TIMEOUT_NS);
+      };
+      auto issued = [&](uint32_t slot) {
+        issued_mask |= 1u << slot;
+        last_parity = (last_parity & ~(1u << slot)) | (((seq / NS) & 1u) << slot);
+        ++seq;
+      };
+      while (ok) {
+        if (!mbar_wait_bounded(smem_u32(&c.lfull[qs]), qph, abort_flag, p.err, TIMEOUT_NS)) {
           ok = false;
           break;
         }
-        if (lane == 0 && rank == 0) mbar_expect_tx(bar(c.full[slot]), tx);
-        __syncwarp();
-        if (active) {
-          if (j == 0) {
+        Tile t;
+        lds_tile(smem_u32(&c.lsq[qs]), t);
+        const uint32_t tq = qs;  // the slot (and its row list) stays held until the tile is issued
+        if (++qs == SQ) { qs = 0; qph ^= 1u; }
+        if (t.prob < 0) {
+          mbar_arrive(smem_u32(&c.lempty[tq]));
+          break;
+        }
+        if (rank == 0) mbar_arrive(bar(c.took));  // the scheduler may claim the next tile
+        const TileBoxes b = tile_boxes<MODE>(p, t, rank);
+        if (gather && !t.shared) {
+          // routed rows gathered from x: the weight box, then one gather4 per four of this
+          // CTA's token rows and unit
+          const int half = t.ncols / 2;
+          const uint32_t tok_bytes = tok_unit_bytes(t, true);
+          const uint32_t sbytes = stage_bytes_of(t, true);
+          const int4* grow = reinterpret_cast<const int4*>(&c.grow[tq][0]);
+          for (int kb = 0; kb < t.kb; ++kb) {
+            const int nu = min(UNITS, t.ku - kb * UNITS);
+            const int kc = t.ku0 + kb * UNITS;
+            // the weight box always brings both units (past the end of K: zeros)
+            const uint32_t tx = 2 * (A_BYTES + nu * tok_bytes);
+            uint32_t off, slot;
+            if (!place_and_wait(sbytes, off, slot)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = mapa_shared(bar(c.full[slot]), 0);
+            const uint32_t sa = sbase + off;
+            if (rank == 0) mbar_expect_tx(bar(c.full[slot]), tx);
+            if (hint) tma_load_5d_pair_hint(sa, b.tw, fb, 0, 0, b.wa, b.wb, kc, pol_w);
+            else tma_load_5d_pair(sa, b.tw, fb, 0, 0, b.wa, b.wb, kc);
+            for (int i = 0; 4 * i < half; ++i) {
+              const int4 r = grow[i];
+              const uint32_t sg = sa + A_BYTES + i * (4 * KU * 2);
+              tma_gather4_pair(sg, &p.tmXg, fb, kc * KU, r.x, r.y, r.z, r.w);
+              if (nu > 1)
+                tma_gather4_pair(sg + tok_bytes, &p.tmXg, fb, (kc + 1) * KU, r.x, r.y, r.z, r.w);
+            }
+            issued(slot);
+          }
+        } else {
+          // Every copy brings both units of the stage (past the end of K: zeros), so each stage
+          // expects its full size.
+          const uint32_t sbytes = stage_bytes_of(t, false);
+          const uint32_t tx = 2 * sbytes;
+          // shared down projection: (ws, wkc) = the shared expert of the stage's first unit
+          // and the unit within its intermediate size (a multiple of 128: no stage straddles
+          // two experts)
+          const bool stacked = MODE == MODE_DOWN && t.shared;
+          const int ipu = stacked ? p.I / KU : 0;
+          int ws = stacked ? t.ku0 / ipu : 0;
+          int wkc = stacked ? t.ku0 - ws * ipu : t.ku0;
+          for (int kb = 0; kb < t.kb; ++kb) {
+            const int kc = t.ku0 + kb * UNITS;
+            const int wrow = b.wa + ws * p.H;
+            uint32_t off, slot;
+            if (!place_and_wait(sbytes, off, slot)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = mapa_shared(bar(c.full[slot]), 0);  // the first CTA's barrier
+            const uint32_t sa = sbase + off;
+            const uint32_t sb = sa + A_BYTES;
+            if (rank == 0) mbar_expect_tx(bar(c.full[slot]), tx);
             if (MODE == MODE_UP) {
-              if (hint) tma_load_5d_pair_hint(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1, pol_w);
-              else tma_load_5d_pair(sa, b.tw, fb, b.ax, 0, 0, b.ay0, b.ay1);
+              if (hint) tma_load_5d_pair_hint(sa, b.tw, fb, 0, 0, b.wa, b.wb, wkc, pol_w);
+              else tma_load_5d_pair(sa, b.tw, fb, 0, 0, b.wa, b.wb, wkc);
             } else {
-              if (hint) tma_load_2d_pair_hint(sa, b.tw, fb, b.ax, b.ay0, pol_w);
-              else tma_load_2d_pair(sa, b.tw, fb, b.ax, b.ay0);
+              if (hint) tma_load_3d_pair_hint(sa, b.tw, fb, 0, wrow, wkc, pol_w);
+              else tma_load_3d_pair(sa, b.tw, fb, 0, wrow, wkc);
+            }
+            if (hint) tma_load_3d_pair_hint(sb, b.tx, fb, 0, b.trow, kc, pol_x);
+            else tma_load_3d_pair(sb, b.tx, fb, 0, b.trow, kc);
+            issued(slot);
+            wkc += UNITS;
+            if (stacked && wkc >= ipu) {
+              wkc -= ipu;
+              ++ws;
             }
           }
-          if (j < t.nbox) {
-            if (hint) tma_load_2d_pair_hint(sb, b.tx, fb, b.bx, by, pol_x);
-            else tma_load_2d_pair(sb, b.tx, fb, b.bx, by);
-          }
         }
-        __syncwarp();
-        issued(slot);
+        mbar_arrive(smem_u32(&c.lempty[tq]));
       }
-    }
-    if (ok && seq > 0) {
-      // tail: wait until the MMA has released the last stage (and with it every earlier one)
-      const uint32_t w = seq - 1;
-      warp_wait_bounded(bar(c.empty[w % NS]), (w / NS) & 1u, abort_flag, p.err, TIMEOUT_NS);
-    }
-    if (*abort_flag && lane == 0) {
-      if (rank == 0) {
-        for (int s = 0; s < NS; ++s)
-          if ((issued_mask >> s) & 1u) grace_wait(bar(c.full[s]), (last_parity >> s) & 1u);
-      } else {
-        grace_sleep();  // this CTA's loads complete on the other CTA's barriers
+      if (ok && seq > 0) {
+        // tail: wait until the MMA has released the last stage (and with it every earlier one)
+        const uint32_t w = seq - 1;
+        mbar_wait_bounded(bar(c.empty[w % NS]), (w / NS) & 1u, abort_flag, p.err, TIMEOUT_NS);
+      }
+      if (*abort_flag) {
+        if (rank == 0) {
+          for (int s = 0; s < NS; ++s)
+            if ((issued_mask >> s) & 1u) grace_wait(bar(c.full[s]), (last_parity >> s) & 1u);
+        } else {
+          grace_sleep();  // this CTA's loads complete on the other CTA's barriers
+        }
       }
     }
   } else if (warp == 1) {
@@ -1136,25 +1119,49 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 row-major tensor [outer, inner] (inner a multiple of 64) viewed as (k, row, unit) =
+// element (row, 64 unit + k): a box (64, rows, 2) brings `rows` rows of two consecutive 64-element
+// units, unit after unit, each a 128-byte-swizzled [rows, 64] tile (the stage layout).
+bool make_unit_pair_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr || base == nullptr || inner == 0 || inner % KU != 0 || outer == 0)
+    return false;
+  cuuint64_t dims[3] = {(cuuint64_t)KU, outer, inner / KU};
+  cuuint64_t strides[2] = {inner * 2, KU * 2};
+  cuuint32_t box[3] = {(cuuint32_t)KU, rows, UNITS};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // UP weights [E, 2I, H] (E experts; rows 0..I-1 gate, I..2I-1 up) as a 5-D tensor
-// (k, r, which, g, e) = element (e, which * I + 16 g + r, k), box (64, 16, 2, 4, 1): one load
-// brings 64 features' gate and up rows interleaved 16 at a time (gate 16, up 16, ...).
+// (k, r, w, g, u) = element (w / 2, (w % 2) * I + 16 g + r, 64 u + k) (w = 2 * expert + gate/up:
+// the two halves of an expert and the experts follow each other at the same stride), box
+// (64, 16, 2, 4, 2): one load brings 64 features' gate and up rows interleaved 16 at a time
+// (gate 16, up 16, ...), for two consecutive 64-element units of the hidden size.
 bool make_up_weight_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t E) {
   auto fn = encode_fn();
-  if (fn == nullptr || base == nullptr || H == 0 || I == 0 || E == 0 || I % 64 != 0) return false;
-  cuuint64_t dims[5] = {H, 16, 2, I / 16, E};
-  cuuint64_t strides[4] = {H * 2, I * H * 2, 16 * H * 2, 2 * I * H * 2};
-  cuuint32_t box[5] = {64, 16, 2, 4, 1};
+  if (fn == nullptr || base == nullptr || H == 0 || H % KU != 0 || I == 0 || I % 64 != 0 ||
+      E == 0)
+    return false;
+  cuuint64_t dims[5] = {(cuuint64_t)KU, 16, 2 * E, I / 16, H / KU};
+  cuuint64_t strides[4] = {H * 2, I * H * 2, 16 * H * 2, KU * 2};
+  cuuint32_t box[5] = {(cuuint32_t)KU, 16, 2, 4, UNITS};
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Token operand [outer, inner] with both box heights.
-bool make_token_maps(CUtensorMap* big, CUtensorMap* small, const void* base, uint64_t inner,
+// Token operand [outer, inner]: the unit-pair maps with boxes of 32, 64 and 128 rows.
+bool make_token_maps(CUtensorMap (&m)[NTOKMAP], const void* base, uint64_t inner,
                      uint64_t outer) {
-  return make_map(big, base, inner, outer, XBOX_L) && make_map(small, base, inner, outer, XBOX_S);
+  bool ok = true;
+  for (int i = 0; i < NTOKMAP; ++i)
+    ok = ok && make_unit_pair_map(&m[i], base, inner, outer, 32u << i);
+  return ok;
 }
 
 // max_pairs > 0 caps the grid at that many CTA pairs.
@@ -1225,7 +1232,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
   const uint64_t H = a.H, I = a.I, S = a.S, N = a.N, T = a.T, R = a.rows_cap;
   bool ok = true;
   if (a.mode == MODE_GATE) {
-    ok = make_map(&prm.tmW0, a.b0, H, N, BM) && make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, T);
+    ok = make_unit_pair_map(&prm.tmW0, a.b0, H, N, BM) && make_token_maps(prm.tmX0, a.a0, H, T);
     if (!ok) return cudaErrorInvalidValue;
     // Few token tiles (decode): split the K range over up to kGateMaxSplits pairs per tile; the
     // partial sums go to the caller's scratch and are reduced in a fixed order. (Measured at
@@ -1264,19 +1271,19 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t st) {
         ok = ok && make_map(&prm.tmXg, a.a0, H, T, 1);  // x [T, H], rows gathered
         prm.row_token = a.row_token;
       } else {
-        ok = ok && make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, H, R);
+        ok = ok && make_token_maps(prm.tmX0, a.a0, H, R);
       }
     }
     if (a.has_shared) ok = ok && make_up_weight_map(&prm.tmW1, a.b1, H, I, S) &&
-                           make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, H, T);
+                           make_token_maps(prm.tmX1, a.a1, H, T);
     if (!ok) return cudaErrorInvalidValue;
     return prm.T <= kDeepRingMaxTokens ? launch_mode<MODE_UP, NSLOT>(prm, num_sms, st)
                                        : launch_mode<MODE_UP, 3>(prm, num_sms, st);
   }
-  if (a.n_routed > 0) ok = ok && make_map(&prm.tmW0, a.b0, I, N * H, BM) &&
-                           make_token_maps(&prm.tmX0, &prm.tmX0s, a.a0, I, R);
-  if (a.has_shared) ok = ok && make_map(&prm.tmW1, a.b1, I, S * H, BM) &&
-                         make_token_maps(&prm.tmX1, &prm.tmX1s, a.a1, S * I, T);
+  if (a.n_routed > 0) ok = ok && make_unit_pair_map(&prm.tmW0, a.b0, I, N * H, BM) &&
+                           make_token_maps(prm.tmX0, a.a0, I, R);
+  if (a.has_shared) ok = ok && make_unit_pair_map(&prm.tmW1, a.b1, I, S * H, BM) &&
+                         make_token_maps(prm.tmX1, a.a1, S * I, T);
   if (!ok) return cudaErrorInvalidValue;
   return prm.T <= kDeepRingMaxTokens ? launch_mode<MODE_DOWN, NSLOT>(prm, num_sms, st)
                                      : launch_mode<MODE_DOWN, 3>(prm, num_sms, st);
