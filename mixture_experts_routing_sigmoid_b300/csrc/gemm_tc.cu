@@ -478,7 +478,7 @@ __device__ __forceinline__ bool ring_publish(SmemCtl& c, uint32_t qs, uint32_t q
   return true;
 }
 
-// First CTA: send `t` to slot `qs` of the second CTA's channel. Warp-wide (producer warp).
+// First CTA: send `t` to slot `qs` of the second CTA's channel. Warp-wide (scheduler warp).
 __device__ __forceinline__ bool ring_send(SmemCtl& c, uint32_t qs, uint32_t qph, const Tile& t,
                                           volatile int* abort_flag, int* err) {
   if (!warp_wait_bounded(smem_u32(&c.xempty[qs]), qph ^ 1u, abort_flag, err, TIMEOUT_NS))
