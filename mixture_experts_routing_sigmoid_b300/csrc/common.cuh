@@ -86,6 +86,17 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// One lane of the (converged) warp: true in exactly one lane.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
+}
+
 // ------------------------------------------------------------------ instruction placement
 // An empty volatile statement that reads v: the compiler computes v before it, and volatile
 // statements keep their order, so placed before an mbarrier wait it keeps the work that v needs

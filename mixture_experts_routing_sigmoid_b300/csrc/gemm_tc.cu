@@ -45,9 +45,12 @@
 //               stream its weights, to about half of what a copy per unit and token box took.
 //               Lane 0 alone walks a tile's stages. Completion of both CTAs' loads is counted
 //               on the first CTA's full barrier; the MMA's commit frees the stage in both CTAs.
-//   warp 1      TMEM owner (both CTAs) and, in the first CTA, MMA issuer: a single thread waits
-//               for each stage and issues its tcgen05.mma (M=256, N=tile's tokens rounded up to
-//               16, K=16; four per unit) into one of two 256-column fp32 accumulators.
+//   warp 1      TMEM owner (both CTAs) and, in the first CTA, MMA issuer: the whole warp waits
+//               for each stage and computes its operands (so they are warp-uniform), and one
+//               elected lane issues its tcgen05.mma (M=256, N=tile's tokens rounded up to 16,
+//               K=16; four per unit) into one of two 256-column fp32 accumulators. (Issued from a
+//               lone lane, a stage of eight MMAs took ~930 cycles of the issuer whatever N, the
+//               bound of every tile with few tokens; warp-wide, decode T = 512 runs 2% faster.)
 //   warps 2..9  epilogue (both CTAs): two warps per quarter of the TMEM lanes (a warp may only
 //               read its own quarter), taking alternate 32-column chunks: tcgen05.ld, SwiGLU /
 //               router bias, stores. Two warps per quarter keep a short tile's epilogue (a few
@@ -515,15 +518,6 @@ __device__ __forceinline__ bool ring_recv(SmemCtl& c, uint32_t qs, uint32_t qph,
   return true;
 }
 
-// Take slot `qs` of this CTA's local ring (one thread).
-__device__ __forceinline__ bool ring_take(SmemCtl& c, uint32_t qs, uint32_t qph, Tile& t,
-                                          volatile int* abort_flag, int* err) {
-  if (!mbar_wait_bounded(smem_u32(&c.lfull[qs]), qph, abort_flag, err, TIMEOUT_NS)) return false;
-  lds_tile(smem_u32(&c.lsq[qs]), t);
-  mbar_arrive(smem_u32(&c.lempty[qs]));
-  return true;
-}
-
 // Warp-wide ring_take: lane 0 waits, every lane reads the slot, lane 0 releases it.
 __device__ __forceinline__ bool ring_take_warp(SmemCtl& c, uint32_t qs, uint32_t qph, Tile& t,
                                                volatile int* abort_flag, int* err) {
@@ -825,20 +819,23 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer (first CTA)
-    if (rank == 0 && lane == 0) {
+    // The whole warp walks the tiles and stages and computes every operand (so the operands are
+    // warp-uniform); one elected lane issues the MMAs and commits.
+    if (rank == 0) {
+      const bool leader = elect_one_sync();
       uint32_t slot = 0, sphase = 0, acc = 0, aphase = 0, qs = 0, qph = 0;
       RingPlace place;
       bool ok = true;
       while (ok) {
         Tile t;
-        if (!ring_take(c, qs, qph, t, abort_flag, p.err)) break;
+        if (!ring_take_warp(c, qs, qph, t, abort_flag, p.err)) break;
         if (++qs == SQ) { qs = 0; qph ^= 1u; }
         if (t.prob < 0) break;
         const uint32_t idesc = idesc_bf16_f32(2 * BM, t.ncols);
         const bool gathered = MODE == MODE_UP && p.row_token != nullptr && !t.shared;
         const uint32_t tok_bytes = tok_unit_bytes(t, gathered);
         const uint32_t sbytes = stage_bytes_of(t, gathered);
-        if (!mbar_wait_bounded(bar(c.tempty[acc]), aphase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
+        if (!warp_wait_bounded(bar(c.tempty[acc]), aphase ^ 1u, abort_flag, p.err, TIMEOUT_NS)) {
           ok = false;
           break;
         }
@@ -853,31 +850,39 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
           const bool two = t.ku - kb * UNITS > 1;
           const uint32_t acc0 = kb > 0 ? 1u : 0u;
           ready_before(ad0); ready_before(bd0); ready_before(ad1); ready_before(bd1);
-          if (!mbar_wait_bounded(bar(c.full[slot]), sphase, abort_flag, p.err, TIMEOUT_NS)) {
+          // every lane polls the barrier; the warp goes on only if all lanes saw the phase end
+          const bool got = mbar_wait_bounded(bar(c.full[slot]), sphase, abort_flag, p.err,
+                                             TIMEOUT_NS);
+          if (!__all_sync(FULL_MASK, got)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < KU / 16; ++kk)
-            tc_mma_f16_pair(d_tmem, ad0 + 2u * kk, bd0 + 2u * kk, idesc, kk > 0 ? 1u : acc0);
-          if (two) {
+          if (leader) {
 #pragma unroll
             for (int kk = 0; kk < KU / 16; ++kk)
-              tc_mma_f16_pair(d_tmem, ad1 + 2u * kk, bd1 + 2u * kk, idesc, 1u);
+              tc_mma_f16_pair(d_tmem, ad0 + 2u * kk, bd0 + 2u * kk, idesc, kk > 0 ? 1u : acc0);
+            if (two) {
+#pragma unroll
+              for (int kk = 0; kk < KU / 16; ++kk)
+                tc_mma_f16_pair(d_tmem, ad1 + 2u * kk, bd1 + 2u * kk, idesc, 1u);
+            }
+            tc_commit_pair_mc(bar(c.empty[slot]), 0x3);
           }
-          tc_commit_pair_mc(bar(c.empty[slot]), 0x3);
+          __syncwarp();
           if (++slot == NS) { slot = 0; sphase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit_pair_mc(bar(c.tfull[acc]), 0x3);
+        if (leader) tc_commit_pair_mc(bar(c.tfull[acc]), 0x3);
+        __syncwarp();
         acc ^= 1u;
         if (acc == 0) aphase ^= 1u;
       }
-      if (*abort_flag) {
+      if (*abort_flag && leader) {
         tc_commit_pair_mc(bar(c.drain), 0x1);  // arrives once every MMA issued above completed
         grace_wait(bar(c.drain), 0);
       }
+      __syncwarp();
     }
   } else if (warp == SCHED_WARP) {
     // ================================================================ tile scheduler
